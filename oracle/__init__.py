@@ -1,0 +1,8 @@
+"""Float64 CPU oracle of the TwoTower denoise step (test infrastructure only).
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import this package.  The CUDA library never links, imports or executes it,
+and it imports nothing from the library.
+"""
+from .twotower import (UnmaskResult, context_rows, decode, denoise_attention,  # noqa: F401
+                       denoise_attention_seq, kv_append, unmask, unmask_seq)

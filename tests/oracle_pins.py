@@ -1,0 +1,389 @@
+"""Checks that pin the float64 oracle to things other than itself.
+
+Each ``check_*`` takes an implementation namespace ``impl`` exposing
+``context_rows``, ``denoise_attention_seq``, ``unmask_seq`` and ``kv_append``
+(the oracle, or a deliberately broken copy of it) and raises AssertionError if
+the implementation disagrees with:
+
+* brute force (pure-Python loops, a different route to the same definition),
+* a library routine in a case that reduces to it (PyTorch's float64
+  ``scaled_dot_product_attention`` on a contiguous, unpaged key set; SciPy's
+  ``softmax`` for the confidence),
+* closed forms (equal keys give the mean of V; a dominant key returns its V row;
+  a single spike of height a over V-1 zeros gives confidence e^a/(e^a+V-1)),
+* invariants (convex combinations, -inf keys change nothing, physical page order
+  is irrelevant, locked positions are never touched, every block finishes).
+
+The decision rules being pinned are the sampling rule and the confidence trick of
+the TwoTower summary (gist.science/de, "Training und Konditionierung — Sampling",
+and "Der Konfidenz-Trick"), the attention visibility of its "Technisches
+Resümee — Architektur" section, and the commit step of its
+"Generierungsprozess" section.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import scipy.special
+import torch
+
+
+# ------------------------------------------------------------------ helpers (no oracle code)
+
+def _paged_from_contiguous(rng, ctx, page_size, extra_pages=2):
+    """Scatter a contiguous [L, Hkv, D] context into a shuffled page pool; unused slots get NaN."""
+    L, Hkv, D = ctx.shape
+    n_own = max(1, -(-L // page_size))
+    num_pages = n_own + extra_pages
+    perm = rng.permutation(num_pages)
+    table = perm[:n_own]
+    pool = np.full((num_pages, Hkv, page_size, D), np.nan)
+    for j in range(L):
+        pool[table[j // page_size], :, j % page_size, :] = ctx[j]
+    return pool, table
+
+
+def _sdpa(q, K, V, scale, G):
+    """PyTorch float64 SDPA. q [S,Hq,D]; K,V [N,Hkv,D] contiguous; KV heads repeated G times."""
+    qt = torch.from_numpy(np.ascontiguousarray(q.transpose(1, 0, 2)))           # [Hq, S, D]
+    kt = torch.from_numpy(np.ascontiguousarray(K.transpose(1, 0, 2))).repeat_interleave(G, 0)
+    vt = torch.from_numpy(np.ascontiguousarray(V.transpose(1, 0, 2))).repeat_interleave(G, 0)
+    o = torch.nn.functional.scaled_dot_product_attention(qt[None], kt[None], vt[None], scale=scale)
+    return o[0].numpy().transpose(1, 0, 2)                                      # [S, Hq, D]
+
+
+def _brute_attention(q, pool_k, pool_v, table, L, page_size, kb, vb, scale):
+    """Pure-Python attention: enumerate the visible keys by scanning the pages, weight each
+    value by exp(score) and divide by the total weight (inputs are small, no overflow).
+    Returns the outputs [S, Hq, D] and log(total weight) [Hq, S]."""
+    S, Hq, D = q.shape
+    Hkv = kb.shape[1]
+    G = Hq // Hkv
+    owner = {}
+    for lp, page in enumerate(table):
+        owner[int(page)] = lp
+    keys = []                       # (k_row, v_row) per visible key, in any order
+    for page in range(pool_k.shape[0]):
+        if page not in owner:
+            continue
+        for slot in range(page_size):
+            pos = owner[page] * page_size + slot
+            if pos < L:
+                keys.append((pool_k[page, :, slot, :], pool_v[page, :, slot, :]))
+    for s in range(S):
+        keys_blk = (kb[s], vb[s])
+        keys.append(keys_blk)
+    out = np.zeros((S, Hq, D))
+    lse = np.zeros((Hq, S))
+    for i in range(S):
+        for h in range(Hq):
+            g = h // G
+            w = []
+            for kr, _ in keys:
+                w.append(math.exp(scale * math.fsum(float(q[i, h, d]) * float(kr[g, d]) for d in range(D))))
+            tot = math.fsum(w)
+            lse[h, i] = math.log(tot)
+            for d in range(D):
+                out[i, h, d] = math.fsum(wj * float(vr[g, d]) for wj, (_, vr) in zip(w, keys)) / tot
+    return out, lse
+
+
+# ------------------------------------------------------------------ attention pins
+
+def check_attention_bruteforce(impl, seed=0):
+    rng = np.random.default_rng(seed)
+    ps = 4
+    for L in (0, 1, 3, 4, 5, 9):
+        S, Hq, Hkv, D = 3, 4, 2, 3
+        q = rng.normal(size=(S, Hq, D))
+        ctx_k = rng.normal(size=(L, Hkv, D))
+        ctx_v = rng.normal(size=(L, Hkv, D))
+        kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+        pk, table = _paged_from_contiguous(rng, ctx_k, ps)
+        pv = np.full_like(pk, np.nan)
+        for j in range(L):
+            pv[table[j // ps], :, j % ps, :] = ctx_v[j]
+        want, want_lse = _brute_attention(q, pk, pv, table, L, ps, kb, vb, 0.7)
+        kc = impl.context_rows(pk, table, L, ps)
+        vc = impl.context_rows(pv, table, L, ps)
+        got, got_lse = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.7)
+        assert np.allclose(got, want, rtol=0, atol=1e-12), (L, np.abs(got - want).max())
+        assert np.allclose(got_lse, want_lse, rtol=0, atol=1e-12), (L, np.abs(got_lse - want_lse).max())
+
+
+def check_attention_sdpa(impl, seed=1):
+    """Against PyTorch's SDPA on the contiguous concatenation [context ; block] (L = 0 is the
+    plain bidirectional in-block attention)."""
+    rng = np.random.default_rng(seed)
+    for L, ps, (S, Hq, Hkv, D) in ((0, 8, (16, 8, 2, 16)), (37, 8, (16, 8, 2, 16)),
+                                   (64, 16, (16, 4, 1, 32)), (5, 4, (2, 6, 3, 5))):
+        q = rng.normal(size=(S, Hq, D))
+        ctx_k, ctx_v = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+        kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+        scale = 1.0 / math.sqrt(D)
+        want = _sdpa(q, np.concatenate([ctx_k, kb]), np.concatenate([ctx_v, vb]), scale, Hq // Hkv)
+        pk, table = _paged_from_contiguous(rng, ctx_k, ps)
+        pv = np.full_like(pk, np.nan)
+        for j in range(L):
+            pv[table[j // ps], :, j % ps, :] = ctx_v[j]
+        got, _ = impl.denoise_attention_seq(q, impl.context_rows(pk, table, L, ps),
+                                            impl.context_rows(pv, table, L, ps), kb, vb, scale)
+        assert np.allclose(got, want, rtol=0, atol=1e-12), (L, np.abs(got - want).max())
+
+
+def check_attention_closed_forms(impl, seed=2):
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D, L = 4, 4, 2, 8, 11
+    q = rng.normal(size=(S, Hq, D))
+    # (1) all keys equal -> uniform weights -> the mean of V over the L+S keys; lse = c + log(L+S)
+    k_all = rng.normal(size=(Hkv, D))
+    kc = np.broadcast_to(k_all, (L, Hkv, D)).copy()
+    kb = np.broadcast_to(k_all, (S, Hkv, D)).copy()
+    vc, vb = rng.normal(size=(L, Hkv, D)), rng.normal(size=(S, Hkv, D))
+    o, lse = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.5)
+    mean_v = np.concatenate([vc, vb]).mean(axis=0)            # [Hkv, D]
+    G = Hq // Hkv
+    for h in range(Hq):
+        assert np.allclose(o[:, h, :], mean_v[h // G][None, :], rtol=0, atol=1e-12)
+        c = 0.5 * (q[:, h, :] @ k_all[h // G])
+        assert np.allclose(lse[h], c + math.log(L + S), rtol=0, atol=1e-12)
+    # (2) one context key scores 60 above every other key for head 0 -> its V row.
+    # Every other key is tiny (|score| < 0.1), so the planted key carries all but
+    # about (L+S) * e^-59.9 of the weight.
+    kc = rng.normal(size=(L, Hkv, D)) * 1e-3
+    kb = rng.normal(size=(S, Hkv, D)) * 1e-3
+    jstar = 7
+    u = rng.normal(size=D)
+    u /= np.linalg.norm(u)
+    q2 = q.copy()
+    q2[:, 0, :] = 10.0 * u
+    kc[jstar, 0, :] = 6.0 * u
+    o, _ = impl.denoise_attention_seq(q2, kc, vc, kb, vb, 1.0)
+    assert np.allclose(o[:, 0, :], vc[jstar, 0, :][None, :], rtol=0, atol=1e-15)
+    # the same key for head G (KV head 1) does not dominate: KV heads are not mixed
+    assert not np.allclose(o[:, G, :], vc[jstar, 1 % Hkv, :][None, :], rtol=0, atol=1e-3)
+
+
+def check_attention_invariants(impl, seed=3):
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D, L = 5, 6, 3, 4, 13
+    q = rng.normal(size=(S, Hq, D)) * 2
+    kc, vc = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+    kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+    o, lse, p = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.9, return_probs=True)
+    # convex combinations of V: weights >= 0 summing to 1, outputs inside the hull per coordinate
+    assert (p >= 0).all() and np.allclose(p.sum(axis=-1), 1.0, rtol=0, atol=1e-13)
+    allv = np.concatenate([vc, vb])
+    G = Hq // Hkv
+    for h in range(Hq):
+        lo, hi = allv[:, h // G].min(axis=0), allv[:, h // G].max(axis=0)
+        assert (o[:, h] >= lo - 1e-12).all() and (o[:, h] <= hi + 1e-12).all()
+    # an extra context key whose score is -inf changes nothing
+    kx = np.concatenate([kc, rng.normal(size=(1, Hkv, D))])
+    vx = np.concatenate([vc, rng.normal(size=(1, Hkv, D)) * 1e6])
+    bias = np.zeros(L + 1 + S)
+    bias[L] = -np.inf
+    o2, lse2 = impl.denoise_attention_seq(q, kx, vx, kb, vb, 0.9, key_bias=bias)
+    assert np.allclose(o2, o, rtol=0, atol=1e-14) and np.allclose(lse2, lse, rtol=0, atol=1e-14)
+    # permuting the context positions (keys with their values) changes nothing: no positional logic
+    perm = rng.permutation(L)
+    o3, _ = impl.denoise_attention_seq(q, kc[perm], vc[perm], kb, vb, 0.9)
+    assert np.allclose(o3, o, rtol=0, atol=1e-13)
+    # the block's own keys are all visible to every block query (bidirectional): the last block
+    # position's key/value influences the first block query
+    vb2 = vb.copy()
+    vb2[-1] += 5.0
+    o4, _ = impl.denoise_attention_seq(q, kc, vc, kb, vb2, 0.9)
+    assert (np.abs(o4[0] - o[0]) > 1e-6).all()
+    # physical page order is irrelevant, and slots past L are never read
+    ps = 4
+    pk, table = _paged_from_contiguous(rng, kc, ps, extra_pages=3)
+    pv = np.full_like(pk, np.nan)
+    for j in range(L):
+        pv[table[j // ps], :, j % ps, :] = vc[j]
+    o5, _ = impl.denoise_attention_seq(q, impl.context_rows(pk, table, L, ps),
+                                       impl.context_rows(pv, table, L, ps), kb, vb, 0.9)
+    assert np.array_equal(o5, o)
+
+
+# ------------------------------------------------------------------ unmasking pins
+
+def _brute_conf(row):
+    m = max(row)
+    z = math.fsum(math.exp(x - m) for x in row)
+    arg = min(i for i, x in enumerate(row) if x == m)
+    return 1.0 / z, arg
+
+
+def check_unmask_closed_forms(impl):
+    V, tau = 1024, 0.9
+    # spike of height a at token k over zeros: conf = e^a / (e^a + V - 1)
+    def spike_height(conf):
+        return math.log(conf * (V - 1) / (1.0 - conf))
+    rows, want_conf = [], []
+    for k, c in ((5, tau + 1e-3), (900, tau - 1e-3), (0, 0.5), (1023, 0.99)):
+        a = spike_height(c)
+        r = np.zeros(V)
+        r[k] = a
+        rows.append(r)
+        want_conf.append(math.exp(a) / (math.exp(a) + V - 1))
+    # all logits equal: conf = 1/V, argmax = 0
+    rows.append(np.full(V, 3.25))
+    want_conf.append(1.0 / V)
+    # two tied maxima: the lower token id wins
+    r = np.zeros(V)
+    r[17] = r[400] = 9.0
+    rows.append(r)
+    want_conf.append(math.exp(9.0) / (2 * math.exp(9.0) + V - 2))
+    lg = np.stack(rows)
+    S = lg.shape[0]
+    res = impl.unmask_seq(lg, np.ones(S, bool), np.full(S, -7), tau, 1, 8)
+    assert np.allclose(res.conf, want_conf, rtol=1e-13, atol=0)
+    assert list(res.argmax) == [5, 900, 0, 1023, 0, 17]
+    assert list(res.committed_now) == [True, False, False, True, False, False]
+    assert list(res.tokens) == [5, -7, -7, 1023, -7, -7]
+    assert not res.fallback
+
+
+def check_unmask_bruteforce(impl, seed=4):
+    rng = np.random.default_rng(seed)
+    for trial in range(6):
+        S, V = 6, 50
+        lg = rng.normal(scale=3.0, size=(S, V))
+        lg[np.arange(S), rng.integers(0, V, S)] += rng.uniform(0, 12, S)
+        lg = np.round(lg * 4) / 4          # coarse grid: exact ties happen
+        masked = rng.random(S) < 0.7
+        masked[0] = True
+        tau = [0.9, 0.3, 0.05, 0.6, 0.999, 0.2][trial]
+        res = impl.unmask_seq(lg, masked, np.arange(S) + 100, tau, 1, 4)
+        conf, arg = {}, {}
+        for p in range(S):
+            if masked[p]:
+                conf[p], arg[p] = _brute_conf([float(x) for x in lg[p]])
+                assert abs(res.conf[p] - conf[p]) <= 1e-14 and res.argmax[p] == arg[p]
+                sm = scipy.special.softmax(lg[p]).max()
+                assert abs(res.conf[p] - sm) <= 1e-13
+        chosen = [p for p in conf if conf[p] >= tau]
+        if not chosen:
+            best = max(conf.values())
+            chosen = [min(p for p in conf if conf[p] == best)]
+        for p in range(S):
+            want_commit = p in chosen
+            assert res.committed_now[p] == want_commit
+            assert res.masked[p] == (masked[p] and not want_commit)
+            assert res.tokens[p] == (arg[p] if want_commit else p + 100)
+
+
+def check_unmask_rules(impl):
+    V = 64
+    base = np.zeros((4, V))
+    # conf < tau everywhere; rows 1 and 2 identical (tie) and most confident -> fallback picks row 1
+    base[0, 3] = 1.0
+    base[1, 9] = 2.0
+    base[2, 9] = 2.0
+    base[3, 5] = 0.5
+    res = impl.unmask_seq(base, np.ones(4, bool), np.full(4, -1), 0.9, 1, 4)
+    assert res.fallback and list(res.committed_now) == [False, True, False, False]
+    assert res.tokens[1] == 9 and res.masked.sum() == 3
+    # at step T every still-masked position is committed, whatever its confidence
+    res = impl.unmask_seq(base, np.array([True, False, True, True]), np.array([-1, 42, -1, -1]),
+                          0.9, 4, 4)
+    assert list(res.committed_now) == [True, False, True, True] and not res.masked.any()
+    assert list(res.tokens) == [3, 42, 9, 5]
+    # locked positions are never read (NaN logits there) and never change
+    lg = base.copy()
+    lg[1] = np.nan
+    res = impl.unmask_seq(lg, np.array([True, False, True, True]), np.array([-1, 42, -1, -1]),
+                          0.9, 1, 4)
+    assert res.tokens[1] == 42 and not res.committed_now[1] and np.isnan(res.conf[1])
+    assert np.isfinite(res.conf[[0, 2, 3]]).all()
+    # several confident positions: exactly the set {conf >= tau} (adaptive count), no fallback
+    lg = np.zeros((5, V))
+    for p, a in enumerate((20.0, 1.0, 30.0, 15.0, 0.0)):
+        lg[p, p] = a
+    res = impl.unmask_seq(lg, np.ones(5, bool), np.full(5, -1), 0.9, 1, 4)
+    want = [math.exp(a) / (math.exp(a) + V - 1) >= 0.9 for a in (20.0, 1.0, 30.0, 15.0, 0.0)]
+    assert list(res.committed_now) == want and not res.fallback
+    # nothing masked: nothing happens
+    res = impl.unmask_seq(lg, np.zeros(5, bool), np.arange(5), 0.9, 2, 4)
+    assert not res.committed_now.any() and list(res.tokens) == list(range(5))
+
+
+def check_block_loop(impl, seed=5):
+    """Every block finishes within T steps, each step commits at least one position and a
+    committed token never changes afterwards."""
+    rng = np.random.default_rng(seed)
+    S, V, T = 16, 256, 6
+    for blk in range(5):
+        masked = np.ones(S, bool)
+        tokens = np.full(S, -1)
+        history = {}
+        for step in range(1, T + 1):
+            lg = rng.normal(scale=3.0, size=(S, V))
+            lg[np.arange(S), rng.integers(0, V, S)] += rng.uniform(0, 12, S)
+            before = masked.sum()
+            res = impl.unmask_seq(lg, masked, tokens, 0.9, step, T)
+            assert res.committed_now.sum() >= 1 and res.masked.sum() == before - res.committed_now.sum()
+            for p, t in history.items():
+                assert res.tokens[p] == t
+            for p in np.nonzero(res.committed_now)[0]:
+                history[int(p)] = int(res.tokens[p])
+            masked, tokens = res.masked, res.tokens
+            if not masked.any():
+                break
+        assert not masked.any()
+
+
+# ------------------------------------------------------------------ append pins
+
+def check_append(impl, seed=6):
+    rng = np.random.default_rng(seed)
+    ps, Hkv, D, S, B = 4, 2, 3, 5, 3
+    lens = np.array([0, 6, 8])
+    maxp = 4
+    num_pages = B * maxp + 1
+    perm = rng.permutation(num_pages)
+    table = perm[: B * maxp].reshape(B, maxp)
+    ctx = [rng.normal(size=(L, Hkv, D)) for L in lens]
+    kp = np.full((num_pages, Hkv, ps, D), np.nan)
+    vp = np.full((num_pages, Hkv, ps, D), np.nan)
+    vctx = [rng.normal(size=(L, Hkv, D)) for L in lens]
+    for b in range(B):
+        for j in range(lens[b]):
+            kp[table[b, j // ps], :, j % ps] = ctx[b][j]
+            vp[table[b, j // ps], :, j % ps] = vctx[b][j]
+    kn, vn = rng.normal(size=(B, S, Hkv, D)), rng.normal(size=(B, S, Hkv, D))
+    active = np.array([True, True, False])
+    kp0, vp0 = kp.copy(), vp.copy()
+    new_len = impl.kv_append(kp, vp, table, lens, kn, vn, ps, active=active)
+    assert list(new_len) == [5, 11, 8]
+    for b in range(B):
+        got_k = impl.context_rows(kp, table[b], int(new_len[b]), ps)
+        want_k = np.concatenate([ctx[b], kn[b]]) if active[b] else ctx[b]
+        assert np.array_equal(got_k, want_k)
+    # inactive sequence and foreign pages untouched (NaN-aware equality)
+    own = set(table[0]) | set(table[1])
+    for page in range(num_pages):
+        if page not in own:
+            assert np.array_equal(kp[page], kp0[page], equal_nan=True)
+    # attention after the append equals SDPA over the contiguous concatenation
+    q = rng.normal(size=(S, 2 * Hkv, D))
+    kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+    b = 1
+    o, _ = impl.denoise_attention_seq(q, impl.context_rows(kp, table[b], 11, ps),
+                                      impl.context_rows(vp, table[b], 11, ps), kb, vb, 0.6)
+    want = _sdpa(q, np.concatenate([ctx[b], kn[b], kb]), np.concatenate([vctx[b], vn[b], vb]), 0.6, 2)
+    assert np.allclose(o, want, rtol=0, atol=1e-12)
+    # a block that does not fit the sequence's pages is refused
+    try:
+        impl.kv_append(kp, vp, table, np.array([14, 0, 0]), kn, vn, ps)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("capacity overflow not detected")
+
+
+ALL_CHECKS = [check_attention_bruteforce, check_attention_sdpa, check_attention_closed_forms,
+              check_attention_invariants, check_unmask_closed_forms, check_unmask_bruteforce,
+              check_unmask_rules, check_block_loop, check_append]

@@ -1,0 +1,54 @@
+"""Hand-worked examples (tests/golden/*.txt) against the float64 oracle."""
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+_ENV = {k: getattr(math, k) for k in ("exp", "log", "e", "sqrt")}
+
+
+def _read(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = line.split(":", 1)
+            out[key.strip()] = [part.strip() for part in val.split(";")]
+    return out
+
+
+def _nums(parts):
+    return np.array([[eval(x, {"__builtins__": {}}, _ENV) for x in p.split()] for p in parts], float)
+
+
+def test_attention_worked_example():
+    g = _read("attention_worked.txt")
+    q = _nums(g["q"]).reshape(1, 1, 2)
+    kc, vc = _nums(g["k_ctx"])[:, None, :], _nums(g["v_ctx"])[:, None, :]
+    kb, vb = _nums(g["k_blk"])[:, None, :], _nums(g["v_blk"])[:, None, :]
+    o, lse = oracle.denoise_attention_seq(q, kc, vc, kb, vb, 1.0)
+    want_o = [eval(x, {"__builtins__": {}}, _ENV) for x in g["o"]]
+    assert np.allclose(o[0, 0], want_o, rtol=1e-15, atol=0)
+    assert abs(lse[0, 0] - eval(g["lse"][0], {"__builtins__": {}}, _ENV)) < 1e-15
+
+
+def test_unmask_worked_example():
+    g = _read("unmask_worked.txt")
+    lg = _nums(g["logits"])
+    want_conf = [eval(x, {"__builtins__": {}}, _ENV) for x in g["conf"]]
+    masked = np.ones(3, bool)
+    tokens = np.full(3, -1)
+    for step in (1, 2, 3):
+        r = oracle.unmask_seq(lg, masked, tokens, 0.9, step, 3)
+        for p in range(3):
+            if masked[p]:
+                assert abs(r.conf[p] - want_conf[p]) < 1e-15
+                assert r.argmax[p] == int(g["argmax"][0].split()[p])
+        assert list(r.committed_now.astype(int)) == [int(x) for x in g[f"step{step}_committed"][0].split()]
+        masked, tokens = r.masked, r.tokens
+    assert list(tokens) == [int(x) for x in g["final_tokens"][0].split()]

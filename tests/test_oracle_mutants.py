@@ -1,0 +1,186 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins catch each one.
+
+The mistakes live only in this file, on the CPU; the oracle itself is untouched.
+"""
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+
+def _attention_mutant(kind):
+    def attn(q, k_ctx, v_ctx, k_blk, v_blk, sm_scale, key_bias=None, return_probs=False):
+        S, Hq, D = q.shape
+        Hkv = k_blk.shape[1]
+        G = Hq // Hkv
+        if kind == "drop_block":
+            K, Vv = k_ctx, v_ctx
+            if K.shape[0] == 0:
+                K, Vv = k_blk[:1], v_blk[:1]
+        elif kind == "drop_context":
+            K, Vv = k_blk, v_blk
+        else:
+            K = np.concatenate([k_ctx, k_blk], axis=0)
+            Vv = np.concatenate([v_ctx, v_blk], axis=0)
+        if kind == "causal_block":
+            pass
+        o = np.empty((S, Hq, D))
+        lse = np.empty((Hq, S))
+        probs = np.empty((Hq, S, K.shape[0])) if return_probs else None
+        for h in range(Hq):
+            g = h % Hkv if kind == "gqa_modulo" else h // G
+            sc = 1.0 if kind == "no_scale" else sm_scale
+            s = sc * (q[:, h, :] @ K[:, g, :].T)
+            if key_bias is not None and kind not in ("drop_block", "drop_context"):
+                s = s + key_bias[None, :]
+            if kind == "causal_block":
+                L = k_ctx.shape[0]
+                for i in range(S):
+                    s[i, L + i + 1:] = -np.inf
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            if kind == "wrong_axis":
+                p = e / e.sum(axis=0, keepdims=True)
+            else:
+                p = e / e.sum(axis=1, keepdims=True)
+            src = K if kind == "k_for_v" else Vv
+            o[:, h, :] = p @ src[:, g, :]
+            z = e.sum(axis=1)
+            lse[h] = np.log(z) if kind == "lse_no_max" else m[:, 0] + np.log(z)
+            if return_probs:
+                probs[h] = p
+        if return_probs:
+            return o, lse, probs
+        return o, lse
+    return attn
+
+
+def _context_rows_mutant(kind):
+    def rows(pool, page_table_row, L, page_size):
+        j = np.arange(L)
+        if kind == "slot_off_by_one":
+            pages = np.asarray(page_table_row)[j // page_size]
+            slots = (j + 1) % page_size
+        elif kind == "physical_order":
+            pages = np.sort(np.asarray(page_table_row))[j // page_size] if L else np.zeros(0, int)
+            slots = j % page_size
+        else:
+            pages = np.asarray(page_table_row)[j // page_size]
+            slots = j % page_size
+        return pool[pages, :, slots, :]
+    return rows
+
+
+def _unmask_mutant(kind):
+    def unmask_seq(logits, masked, tokens, tau, step, T):
+        S = masked.shape[0]
+        masked = np.asarray(masked, dtype=bool)
+        conf = np.full(S, np.nan)
+        arg = np.full(S, -1, dtype=np.int64)
+        for p in range(S):
+            if not masked[p] and kind != "reread_locked":
+                continue
+            row = np.asarray(logits[p], dtype=np.float64)
+            m = row.max()
+            z = np.exp(row - m).sum()
+            conf[p] = (np.exp(m) / z) if kind == "conf_wrong" else 1.0 / z
+            if kind == "argmax_last":
+                arg[p] = int(len(row) - 1 - np.argmax(row[::-1]))
+            else:
+                arg[p] = int(np.argmax(row))
+        cand = [p for p in range(S) if masked[p]]
+        chosen = [p for p in cand if conf[p] >= tau]
+        fallback = False
+        if step >= T and kind != "no_step_T":
+            chosen = cand
+        elif not chosen and cand and kind != "no_fallback":
+            best = cand[0]
+            for p in cand[1:]:
+                if (conf[p] >= conf[best]) if kind == "fallback_last_tie" else (conf[p] > conf[best]):
+                    best = p
+            if kind == "fallback_least":
+                best = min(cand, key=lambda p: conf[p])
+            chosen = [best]
+            fallback = True
+        new_tokens = np.array(tokens, dtype=np.int64, copy=True)
+        new_masked = masked.copy()
+        committed = np.zeros(S, dtype=bool)
+        for p in chosen:
+            if kind != "no_token_write":
+                new_tokens[p] = arg[p]
+            new_masked[p] = False
+            committed[p] = True
+        if kind == "reread_locked":
+            for p in range(S):
+                if not masked[p] and np.isfinite(conf[p]) and conf[p] >= tau:
+                    new_tokens[p] = arg[p]
+        return oracle.UnmaskResult(new_tokens, new_masked, committed, conf, arg, fallback)
+    return unmask_seq
+
+
+def _append_mutant(kind):
+    def kv_append(k_pool, v_pool, page_table, ctx_len, k_new, v_new, page_size, active=None):
+        B, S = k_new.shape[:2]
+        new_len = np.array(ctx_len, dtype=np.int64, copy=True)
+        for b in range(B):
+            if active is not None and not active[b] and kind != "ignore_active":
+                continue
+            L = int(ctx_len[b])
+            if L + S > page_table.shape[1] * page_size and kind != "no_capacity_check":
+                raise ValueError("block does not fit")
+            for s in range(S):
+                j = L + s + (1 if kind == "slot_shift" else 0)
+                if j >= page_table.shape[1] * page_size:
+                    continue
+                page = page_table[b, j // page_size]
+                k_pool[page, :, j % page_size, :] = k_new[b, s]
+                v_pool[page, :, j % page_size, :] = (k_new if kind == "k_into_v" else v_new)[b, s]
+            new_len[b] = L if kind == "no_len_update" else L + S
+        return new_len
+    return kv_append
+
+
+def _impl(**override):
+    ns = types.SimpleNamespace(context_rows=oracle.context_rows,
+                               denoise_attention_seq=oracle.denoise_attention_seq,
+                               unmask_seq=oracle.unmask_seq, kv_append=oracle.kv_append)
+    for k, v in override.items():
+        setattr(ns, k, v)
+    return ns
+
+
+MUTANTS = (
+    [("attn_" + k, dict(denoise_attention_seq=_attention_mutant(k)))
+     for k in ("gqa_modulo", "drop_block", "drop_context", "no_scale", "wrong_axis", "k_for_v",
+               "lse_no_max", "causal_block")]
+    + [("rows_" + k, dict(context_rows=_context_rows_mutant(k)))
+       for k in ("slot_off_by_one", "physical_order")]
+    + [("unmask_" + k, dict(unmask_seq=_unmask_mutant(k)))
+       for k in ("conf_wrong", "argmax_last", "no_step_T", "no_fallback", "fallback_last_tie",
+                 "fallback_least", "no_token_write", "reread_locked")]
+    + [("append_" + k, dict(kv_append=_append_mutant(k)))
+       for k in ("ignore_active", "no_capacity_check", "slot_shift", "k_into_v", "no_len_update")]
+)
+
+
+def test_unmutated_copy_passes():
+    impl = _impl(denoise_attention_seq=_attention_mutant("none"),
+                 context_rows=_context_rows_mutant("none"), unmask_seq=_unmask_mutant("none"),
+                 kv_append=_append_mutant("none"))
+    for check in oracle_pins.ALL_CHECKS:
+        check(impl)
+
+
+@pytest.mark.parametrize("name,override", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, override):
+    impl = _impl(**override)
+    caught = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(impl)
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            caught.append(check.__name__)
+    assert caught, f"mutant {name} passed every pin"
