@@ -1,0 +1,500 @@
+"""Benchmark of one TwoTower denoiser step on B300: two-segment attention + confidence unmasking.
+
+A step is one pass of the whole hot path over one batch: attention of the S=16 block
+queries of every sequence against its paged context KV and its own block KV (one
+layer), followed by the unmasking of the block over the V=131072 logits.  The default
+workload is the 8K-context batch: B=32 sequences of 8192 context tokens each, 64-token
+pages in shuffled order, 32 query / 2 KV heads, head_dim 128, bf16.  All inputs are
+seeded synthetic tensors resident in HBM before timing starts; two copies of the KV
+pools and logits alternate between steps, so nothing a step reads is left in L2 by the
+step before it (one copy of a step's inputs, 405 MB, is already over 3x the L2).
+
+Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle instead, on a
+bounded sample of the same workload.  Under torchrun each rank runs its own batch
+(sequences are independent: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_wise_diffusion_denoise_b300 import synth  # noqa: E402
+
+WORKLOADS = {
+    "ctx8k": "ctx8k", "single": "single", "ragged": "ragged", "long": "long",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="ctx8k")
+    ap.add_argument("--no-graph", action="store_true", help="launch every step from Python")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- algorithmic cost
+
+def attn_bytes(cfg, lens) -> float:
+    """Bytes a perfect attention kernel moves: context K/V once, q, block K/V and the output."""
+    elem = 2 if cfg.dtype == "bf16" else 4
+    per_seq_fixed = (cfg.S * cfg.Hq * cfg.D * 2 + cfg.S * cfg.Hkv * cfg.D * 2) * elem
+    return float(sum(2 * int(L) * cfg.Hkv * cfg.D * elem for L in lens) + cfg.B * per_seq_fixed)
+
+
+def attn_flops(cfg, lens) -> float:
+    return float(sum(4.0 * cfg.Hq * cfg.S * cfg.D * (int(L) + cfg.S) for L in lens))
+
+
+def unmask_bytes(cfg, masked_rows) -> float:
+    elem = 2 if cfg.dtype == "bf16" else 4
+    return float(masked_rows * cfg.V * elem)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Polls NVML for the SM clock and throttle reasons from a thread while the timed region runs."""
+    REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, index: int):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            pr = torch.cuda.get_device_properties(index)
+            try:   # match the CUDA device to its NVML handle by PCI address
+                bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # NVML absent: report it instead of a clock
+            self.err = repr(e)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for name, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "err", "")}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+class OracleSampler:
+    """Times the float64 oracle on a bounded sample of the workload: (sequence, KV head)
+    attention pairs and single unmask rows, scaled to one full batch step."""
+
+    def __init__(self, cfg, seed):
+        import oracle
+        self.oracle, self.cfg = oracle, cfg
+        self.lens = synth.draw_lengths(cfg, seed)
+        self.cache = synth.draw_paged_cache(cfg, self.lens, int(self.lens.max()) + cfg.S, seed=seed)
+        self.q, self.kb, self.vb = synth.draw_block_qkv(cfg, seed=seed)
+        self.lg = synth.draw_logits(cfg, seed=seed, rows=1)
+        self.n_pairs = self.n_rows = 0
+        self.t_attn = self.t_unm = 0.0
+
+    def one(self):
+        """One attention pair and one unmask row; returns their seconds."""
+        cfg, o, c = self.cfg, self.oracle, self.cache
+        b = (self.n_pairs // cfg.Hkv) % cfg.B
+        g = self.n_pairs % cfg.Hkv
+        L = int(self.lens[b])
+        t0 = time.perf_counter()
+        kc = o.decode(o.context_rows(c.k_pool, c.page_table[b], L, cfg.page_size), cfg.dtype)
+        vc = o.decode(o.context_rows(c.v_pool, c.page_table[b], L, cfg.page_size), cfg.dtype)
+        hs = slice(g * cfg.G, (g + 1) * cfg.G)
+        o.denoise_attention_seq(o.decode(self.q[b][:, hs], cfg.dtype), kc[:, g:g + 1], vc[:, g:g + 1],
+                                o.decode(self.kb[b][:, g:g + 1], cfg.dtype),
+                                o.decode(self.vb[b][:, g:g + 1], cfg.dtype), 1.0 / math.sqrt(cfg.D))
+        t1 = time.perf_counter()
+        masked = np.zeros((1, cfg.S), np.uint8)
+        masked[0, self.n_rows % cfg.S] = 1
+        o.unmask(self.lg, masked, np.full((1, cfg.S), -1), cfg.tau, 1, cfg.T, cfg.dtype)
+        t2 = time.perf_counter()
+        self.n_pairs += 1
+        self.n_rows += 1
+        self.t_attn += t1 - t0
+        self.t_unm += t2 - t1
+        return t1 - t0, t2 - t1
+
+    def scale(self, t_pair, t_row):
+        """Seconds of one full batch step from the time of one pair and one row."""
+        return t_pair * self.cfg.B * self.cfg.Hkv + t_row * self.cfg.B * self.cfg.S
+
+    def run(self, budget_s):
+        t_end = time.perf_counter() + budget_s
+        while time.perf_counter() < t_end or self.n_pairs == 0:
+            self.one()
+        per_step = self.scale(self.t_attn / self.n_pairs, self.t_unm / self.n_rows)
+        return per_step, self.t_attn + self.t_unm
+
+    def note(self):
+        cfg = self.cfg
+        return (f"{self.n_pairs} (sequence, KV head) attention pairs and {self.n_rows} unmask rows of the "
+                f"{cfg.name} workload, scaled to the full batch of {cfg.B} x {cfg.Hkv} pairs and "
+                f"{cfg.B * cfg.S} rows")
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        th = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        th = os.cpu_count()
+    return int(th)
+
+
+def run_reference(a, cfg):
+    """The oracle arm: every step times one attention pair and one unmask row of the
+    workload on the host cores and scales them to one full batch step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    smp = OracleSampler(cfg, a.seed)
+    for _ in range(a.warmup):
+        smp.one()
+    t0 = time.perf_counter()
+    steps = [smp.scale(*smp.one()) for _ in range(a.steps)]
+    wall = time.perf_counter() - t0
+    per_step = sum(steps) / len(steps)
+    value = 1.0 / per_step
+    note = (f"per step, one (sequence, KV head) attention pair and one unmask row of the {cfg.name} "
+            f"workload, scaled to {cfg.B} x {cfg.Hkv} pairs and {cfg.B * cfg.S} rows")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(cfg, a), "wall_s": wall,
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": note},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+METRIC = "denoise steps/s (attn+unmask) at ctx 8K, S=16; % of HBM/tensor roofline"
+
+
+def config_dict(cfg, a):
+    return {"workload": f"{cfg.name}: B={cfg.B}, context {cfg.len_lo}"
+                        + (f"-{cfg.len_hi}" if cfg.len_hi != cfg.len_lo else "")
+                        + f", S={cfg.S}, {cfg.Hq}q/{cfg.Hkv}kv heads, head_dim {cfg.D}, vocab {cfg.V}, "
+                          f"{cfg.page_size}-token shuffled pages, tau={cfg.tau}, one attention layer + unmask per step",
+            "global_batch": cfg.B * a.gpus, "seq_len": cfg.len_hi, "block": cfg.S,
+            "parallelism": f"dp{a.gpus} (independent sequences)",
+            "l2": "inputs larger than L2, two copies alternate between steps"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_ours(a, cfg):
+    import torch
+    import torch.distributed as dist
+
+    from block_wise_diffusion_denoise_b300 import api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    # ---- inputs, resident in HBM; rank r draws its own batch (independent sequences)
+    seed = a.seed + 1000 * rank
+    lens = synth.draw_lengths(cfg, seed)
+    cap = int(lens.max()) + cfg.S
+    cache_h = synth.draw_paged_cache(cfg, lens, cap, seed=seed)
+    q_h, kb_h, vb_h = synth.draw_block_qkv(cfg, seed=seed)
+    lg_h = synth.draw_logits(cfg, seed=seed)
+
+    def dev_t(x):
+        if cfg.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(x).to(dev)
+
+    n_copies = 2
+    base = {"k": dev_t(cache_h.k_pool), "v": dev_t(cache_h.v_pool), "lg": dev_t(lg_h)}
+    table = torch.from_numpy(cache_h.page_table).to(dev)
+    ctx_len = torch.from_numpy(cache_h.ctx_len).to(dev)
+    copies = []
+    for c in range(n_copies):
+        k = base["k"] if c == 0 else base["k"].clone()
+        v = base["v"] if c == 0 else base["v"].clone()
+        lg = base["lg"] if c == 0 else base["lg"].clone()
+        copies.append({"cache": api.KVCache(k, v, table, ctx_len), "q": dev_t(q_h), "kb": dev_t(kb_h),
+                       "vb": dev_t(vb_h), "lg": lg, "out": torch.empty(q_h.shape, dtype=base["k"].dtype,
+                                                                        device=dev)})
+    tdt = base["k"].dtype
+    ws = api.workspace(api.tt_block_step_workspace_size(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.D, cfg.V, tdt), dev)
+    attn_ws = api.workspace(api.tt_denoise_attn_workspace_size(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.D, tdt), dev)
+    unm_ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, tdt), dev)
+    err = api.error_word(dev)
+    n_state = a.warmup + a.steps
+    # every step starts a fresh block (all 16 positions masked, step 1): fresh state per step
+    masked = torch.ones((n_state, cfg.B, cfg.S), dtype=torch.uint8, device=dev)
+    tokens = torch.full((n_state, cfg.B, cfg.S), -1, dtype=torch.int32, device=dev)
+    committed = torch.zeros((n_state, cfg.B, cfg.S), dtype=torch.uint8, device=dev)
+    n_masked = torch.zeros((n_state, cfg.B), dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(cfg.D)
+
+    def step(i, stream=None):
+        c = copies[i % n_copies]
+        api.tt_block_step([c["cache"]], [c["q"]], [c["kb"]], [c["vb"]], [c["out"]], c["lg"], masked[i],
+                          tokens[i], cfg.tau, 1, cfg.T, sm_scale=scale, committed_now=committed[i],
+                          n_masked=n_masked[i], ws=ws, dev_err=err, stream=stream)
+
+    def attn_only(i, stream=None):
+        c = copies[i % n_copies]
+        api.tt_denoise_attn(c["cache"], c["q"], c["kb"], c["vb"], out=c["out"], sm_scale=scale, ws=attn_ws,
+                            dev_err=err, stream=stream)
+
+    unm_masked = torch.ones((n_state, cfg.B, cfg.S), dtype=torch.uint8, device=dev)
+    unm_tokens = torch.full((n_state, cfg.B, cfg.S), -1, dtype=torch.int32, device=dev)
+
+    def unmask_only(i, stream=None):
+        c = copies[i % n_copies]
+        api.tt_unmask(c["lg"], unm_masked[i], unm_tokens[i], cfg.tau, 1, cfg.T, ws=unm_ws, dev_err=err,
+                      stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, first, count, use_graph):
+        """Run fn(first .. first+count-1) and return (ms total) by CUDA events on the launching stream."""
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(first, first + count):
+                    fn(i, stream=s)
+            barrier()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                ev0.record(s)
+                g.replay()
+                ev1.record(s)
+        else:
+            barrier()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(s)
+            for i in range(first, first + count):
+                fn(i, stream=s)
+            ev1.record(s)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1)
+
+    use_graph = not a.no_graph
+    # ---- warm-up (eager), then the timed region: exactly K steps
+    for i in range(a.warmup):
+        step(i)
+    barrier()
+    masked[a.warmup:].fill_(1)
+    sampler = ClockSampler(local)
+    if use_graph:
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(a.warmup, a.warmup + a.steps):
+                step(i, stream=s)
+        masked[a.warmup:].fill_(1)
+        tokens[a.warmup:].fill_(-1)
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with sampler:
+            ev0.record(s)
+            g.replay()
+            ev1.record(s)
+            ev1.synchronize()
+    else:
+        s = torch.cuda.current_stream()
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with sampler:
+            ev0.record(s)
+            for i in range(a.warmup, a.warmup + a.steps):
+                step(i)
+            ev1.record(s)
+            ev1.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    code = api.tt_get_device_error(err)
+    if code != 0:
+        raise SystemExit(f"device error {code} during the timed region")
+    # the timed steps really unmasked: every sequence committed at least one position
+    if int(committed[a.warmup:].sum(dim=2).min().item()) < 1:
+        raise SystemExit("a timed step committed nothing")
+
+    # ---- per-kernel durations (CUDA events on the launching stream), same rotation of inputs
+    k_ker = max(10, min(a.steps, 200))
+    attn_ms = timed(attn_only, 0, k_ker, use_graph) / k_ker
+    unm_masked.fill_(1)
+    unmask_ms = timed(unmask_only, 0, k_ker, use_graph) / k_ker
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the region
+    e2e = None
+    if a.e2e_steps > 0:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        c0 = copies[0]
+        h_q, h_kb, h_vb, h_lg = pin(c0["q"]), pin(c0["kb"]), pin(c0["vb"]), pin(c0["lg"])
+        h_out = torch.empty(c0["out"].shape, dtype=c0["out"].dtype).pin_memory()
+        h_tok = torch.empty((cfg.B, cfg.S), dtype=torch.int32).pin_memory()
+        h_msk = torch.empty((cfg.B, cfg.S), dtype=torch.uint8).pin_memory()
+        h_msk_in = torch.ones((cfg.B, cfg.S), dtype=torch.uint8).pin_memory()
+        h_tok_in = torch.full((cfg.B, cfg.S), -1, dtype=torch.int32).pin_memory()
+        d = {k: torch.empty_like(v, device=dev) for k, v in
+             (("q", h_q), ("kb", h_kb), ("vb", h_vb), ("lg", h_lg))}
+        d_m = torch.empty((cfg.B, cfg.S), dtype=torch.uint8, device=dev)
+        d_t = torch.empty((cfg.B, cfg.S), dtype=torch.int32, device=dev)
+        d_o = torch.empty_like(c0["out"])
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kb, h_vb, h_lg, h_msk_in, h_tok_in))
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_tok, h_msk))
+
+        def e2e_step():
+            for k, h in (("q", h_q), ("kb", h_kb), ("vb", h_vb), ("lg", h_lg)):
+                d[k].copy_(h, non_blocking=True)
+            d_m.copy_(h_msk_in, non_blocking=True)
+            d_t.copy_(h_tok_in, non_blocking=True)
+            api.tt_block_step([c0["cache"]], [d["q"]], [d["kb"]], [d["vb"]], [d_o], d["lg"], d_m, d_t, cfg.tau,
+                              1, cfg.T, sm_scale=scale, ws=ws, dev_err=err)
+            h_out.copy_(d_o, non_blocking=True)
+            h_tok.copy_(d_t, non_blocking=True)
+            h_msk.copy_(d_m, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(a.e2e_steps):
+            e2e_step()
+        e1.record()
+        e1.synchronize()
+        e_ms = e0.elapsed_time(e1) / a.e2e_steps
+        et = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e = {"value": world / (float(et.item()) / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": a.e2e_steps}
+
+    if rank == 0:
+        import json as _json
+        peaks = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+            if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        hbm = peaks.get("hbm_gbs", 6400.0)
+        tc = peaks.get("bf16_tflops", 1800.0)
+        src = "of measured" if peaks else "of fallback"
+        ab, af = attn_bytes(cfg, lens), attn_flops(cfg, lens)
+        ub = unmask_bytes(cfg, cfg.B * cfg.S)
+        attn_gbs = ab / (attn_ms * 1e-3) / 1e9
+        attn_tfs = af / (attn_ms * 1e-3) / 1e12
+        unm_gbs = ub / (unmask_ms * 1e-3) / 1e9
+        step_roof_us = max(ab / (hbm * 1e9), af / (tc * 1e12)) * 1e6 + ub / (hbm * 1e9) * 1e6
+        value = world * a.steps / (ms / 1e3)
+        line = {
+            "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded; value distributions of the "
+                                                              "workload recipe)",
+            "config": config_dict(cfg, a),
+            "roofline": {"bound": "hbm", "kernel": "denoise attention", "achieved": attn_gbs, "peak": hbm,
+                         "unit": "GB/s", "frac": attn_gbs / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": ab, "avg_launch_us": attn_ms * 1e3,
+                         "tensor_tflops": attn_tfs, "tensor_frac": attn_tfs / tc,
+                         "traffic": None},
+            "kernels": {
+                "attention": {"us": attn_ms * 1e3, "gbs": attn_gbs, "hbm_frac": attn_gbs / hbm,
+                              "roofline_us": max(ab / (hbm * 1e9), af / (tc * 1e12)) * 1e6},
+                "unmask": {"us": unmask_ms * 1e3, "gbs": unm_gbs, "hbm_frac": unm_gbs / hbm,
+                           "roofline_us": ub / (hbm * 1e9) * 1e6},
+                "step_roofline_us": step_roof_us, "step_frac": step_roof_us / (ms / a.steps * 1e3)},
+            "gpu_launches": a.steps * launches_per_step(cfg),
+            "graph": use_graph,
+            "clocks": sampler.summary(),
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        if not a.no_cpu_baseline:
+            smp = OracleSampler(cfg, a.seed)
+            per_step, spent = smp.run(12.0)
+            line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": cpu_cores(),
+                                    "kind": "oracle", "sample": smp.note() + f" ({spent:.1f} s of CPU time)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def launches_per_step(cfg) -> int:
+    return 2          # one attention kernel + one unmask kernel
+
+
+def main():
+    a = parse()
+    cfg = synth.CONFIGS[WORKLOADS[a.config]]
+    if a.impl == "reference":
+        return run_reference(a, cfg)
+    return run_ours(a, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

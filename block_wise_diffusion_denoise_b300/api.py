@@ -1,0 +1,250 @@
+"""Thin PyTorch binding of the C ABI (argument marshalling only).
+
+Every function here checks that its tensors are contiguous CUDA tensors of the
+expected dtype, passes their ``data_ptr()`` and the current CUDA stream to the
+library, and raises ``TTError`` on a non-zero status.  All arithmetic of the
+denoise step runs in the library's CUDA kernels; PyTorch only provides device
+memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _native as N
+from ._native import TT_BF16, TT_FP32, TTError  # noqa: F401
+
+_DT = {torch.bfloat16: TT_BF16, torch.float32: TT_FP32}
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+@dataclasses.dataclass
+class KVCache:
+    """One attention layer's paged context KV cache (device tensors).
+
+    k_pool, v_pool: [num_pages, Hkv, page_size, D] (bf16 or fp32);
+    page_table: [B, max_pages_per_seq] int32; ctx_len: [B] int32."""
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    page_table: torch.Tensor
+    ctx_len: torch.Tensor
+
+    def __post_init__(self):
+        if self.k_pool.dtype not in _DT or self.v_pool.dtype != self.k_pool.dtype:
+            raise ValueError("k_pool / v_pool must both be bf16 or both fp32")
+        if self.k_pool.dim() != 4 or self.v_pool.shape != self.k_pool.shape:
+            raise ValueError("pools must be [num_pages, Hkv, page_size, D] and equal in shape")
+        _need(self.k_pool, "k_pool")
+        _need(self.v_pool, "v_pool")
+        _need(self.page_table, "page_table", torch.int32)
+        _need(self.ctx_len, "ctx_len", torch.int32)
+        if self.page_table.dim() != 2 or self.ctx_len.dim() != 1 or \
+                self.ctx_len.shape[0] != self.page_table.shape[0]:
+            raise ValueError("page_table must be [B, max_pages] and ctx_len [B]")
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.k_pool.dtype
+
+    @property
+    def n_kv_heads(self) -> int:
+        return int(self.k_pool.shape[1])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.k_pool.shape[2])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.k_pool.shape[3])
+
+    def struct(self) -> N.tt_kv_cache:
+        c = N.tt_kv_cache()
+        c.k_pool = self.k_pool.data_ptr()
+        c.v_pool = self.v_pool.data_ptr()
+        c.page_table = self.page_table.data_ptr()
+        c.ctx_len = self.ctx_len.data_ptr()
+        c.num_pages = int(self.k_pool.shape[0])
+        c.max_pages_per_seq = int(self.page_table.shape[1])
+        c.page_size = self.page_size
+        c.n_kv_heads = self.n_kv_heads
+        c.head_dim = self.head_dim
+        c.dtype = _DT[self.dtype]
+        return c
+
+
+# ----------------------------------------------------------------------------- workspace
+
+def tt_denoise_attn_workspace_size(B: int, S: int, Hq: int, Hkv: int, D: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    N.check(N.lib().tt_denoise_attn_workspace_size(B, S, Hq, Hkv, D, _DT[dtype], ctypes.byref(n)),
+            "tt_denoise_attn_workspace_size")
+    return int(n.value)
+
+
+def tt_unmask_workspace_size(B: int, S: int, V: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    N.check(N.lib().tt_unmask_workspace_size(B, S, V, _DT[dtype], ctypes.byref(n)), "tt_unmask_workspace_size")
+    return int(n.value)
+
+
+def tt_block_step_workspace_size(B: int, S: int, Hq: int, Hkv: int, D: int, V: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    N.check(N.lib().tt_block_step_workspace_size(B, S, Hq, Hkv, D, V, _DT[dtype], ctypes.byref(n)),
+            "tt_block_step_workspace_size")
+    return int(n.value)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace buffer (the library requires zeros before first use)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def error_word(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+# ----------------------------------------------------------------------------- calls
+
+def tt_denoise_attn(cache: KVCache, q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                    sm_scale: Optional[float] = None, max_ctas: int = 0,
+                    ws: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Two-segment attention of one layer; q [B,S,Hq,D], k_blk/v_blk [B,S,Hkv,D] -> out [B,S,Hq,D]."""
+    B, S, Hq, D = q.shape
+    Hkv = cache.n_kv_heads
+    _need(q, "q", cache.dtype)
+    _need(k_blk, "k_blk", cache.dtype, (B, S, Hkv, D))
+    _need(v_blk, "v_blk", cache.dtype, (B, S, Hkv, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", cache.dtype, q.shape)
+    _need(lse, "lse", torch.float32, (B, Hq, S), allow_none=True)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if ws is None:
+        ws = workspace(tt_denoise_attn_workspace_size(B, S, Hq, Hkv, D, cache.dtype), q.device)
+    st = cache.struct()
+    N.check(N.lib().tt_denoise_attn(ctypes.byref(st), q.data_ptr(), k_blk.data_ptr(), v_blk.data_ptr(),
+                                    out.data_ptr(), _ptr(lse), B, S, Hq, float(sm_scale), int(max_ctas),
+                                    ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+            "tt_denoise_attn")
+    return out
+
+
+def tt_unmask(logits: torch.Tensor, masked: torch.Tensor, tokens: torch.Tensor, tau: float, step: int, T: int,
+              committed_now: Optional[torch.Tensor] = None, conf: Optional[torch.Tensor] = None,
+              n_masked: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+              dev_err: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Confidence unmasking in place: logits [B,S,V]; masked [B,S] uint8; tokens [B,S] int32."""
+    B, S, V = logits.shape
+    if logits.dtype not in _DT:
+        raise ValueError("logits must be bf16 or fp32")
+    _need(logits, "logits")
+    _need(masked, "masked", torch.uint8, (B, S))
+    _need(tokens, "tokens", torch.int32, (B, S))
+    _need(committed_now, "committed_now", torch.uint8, (B, S), allow_none=True)
+    _need(conf, "conf", torch.float32, (B, S), allow_none=True)
+    _need(n_masked, "n_masked", torch.int32, (B,), allow_none=True)
+    if ws is None:
+        ws = workspace(tt_unmask_workspace_size(B, S, V, logits.dtype), logits.device)
+    N.check(N.lib().tt_unmask(logits.data_ptr(), _DT[logits.dtype], B, S, V, float(tau), int(step), int(T),
+                              masked.data_ptr(), tokens.data_ptr(), _ptr(committed_now), _ptr(conf),
+                              _ptr(n_masked), ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+            "tt_unmask")
+
+
+def tt_kv_append(caches: Sequence[KVCache], k_new: Sequence[torch.Tensor], v_new: Sequence[torch.Tensor],
+                 seq_active: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Append one block per layer (k_new[l], v_new[l]: [B,S,Hkv,D]) and advance the shared ctx_len once."""
+    n = len(caches)
+    if n == 0 or len(k_new) != n or len(v_new) != n:
+        raise ValueError("one k_new / v_new per cache")
+    B, S = k_new[0].shape[:2]
+    for l in range(n):
+        shp = (B, S, caches[l].n_kv_heads, caches[l].head_dim)
+        _need(k_new[l], f"k_new[{l}]", caches[l].dtype, shp)
+        _need(v_new[l], f"v_new[{l}]", caches[l].dtype, shp)
+    _need(seq_active, "seq_active", torch.uint8, (B,), allow_none=True)
+    structs = (N.tt_kv_cache * n)(*[c.struct() for c in caches])
+    N.check(N.lib().tt_kv_append(structs, n, N.ptr_array([t.data_ptr() for t in k_new]),
+                                 N.ptr_array([t.data_ptr() for t in v_new]), _ptr(seq_active), B, S,
+                                 _ptr(dev_err), _stream(stream)),
+            "tt_kv_append")
+
+
+def tt_block_step(caches: Sequence[KVCache], q: Sequence[torch.Tensor], k_blk: Sequence[torch.Tensor],
+                  v_blk: Sequence[torch.Tensor], out: Sequence[torch.Tensor], logits: torch.Tensor,
+                  masked: torch.Tensor, tokens: torch.Tensor, tau: float, step: int, T: int,
+                  sm_scale: Optional[float] = None, committed_now: Optional[torch.Tensor] = None,
+                  conf: Optional[torch.Tensor] = None, n_masked: Optional[torch.Tensor] = None,
+                  ws: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """One denoiser step: attention for every layer, then unmasking of the step's logits."""
+    n = len(caches)
+    if not (len(q) == len(k_blk) == len(v_blk) == len(out) == n) or n == 0:
+        raise ValueError("one q / k_blk / v_blk / out per layer")
+    B, S, Hq, D = q[0].shape
+    V = logits.shape[2]
+    dt = caches[0].dtype
+    for l in range(n):
+        _need(q[l], f"q[{l}]", dt, (B, S, Hq, D))
+        _need(k_blk[l], f"k_blk[{l}]", dt, (B, S, caches[l].n_kv_heads, D))
+        _need(v_blk[l], f"v_blk[{l}]", dt, (B, S, caches[l].n_kv_heads, D))
+        _need(out[l], f"out[{l}]", dt, (B, S, Hq, D))
+    _need(logits, "logits", dt, (B, S, V))
+    _need(masked, "masked", torch.uint8, (B, S))
+    _need(tokens, "tokens", torch.int32, (B, S))
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if ws is None:
+        ws = workspace(tt_block_step_workspace_size(B, S, Hq, caches[0].n_kv_heads, D, V, dt), logits.device)
+    structs = (N.tt_kv_cache * n)(*[c.struct() for c in caches])
+    N.check(N.lib().tt_block_step(structs, n, N.ptr_array([t.data_ptr() for t in q]),
+                                  N.ptr_array([t.data_ptr() for t in k_blk]),
+                                  N.ptr_array([t.data_ptr() for t in v_blk]),
+                                  N.ptr_array([t.data_ptr() for t in out]), logits.data_ptr(), B, S, Hq, V,
+                                  float(tau), int(step), int(T), float(sm_scale), masked.data_ptr(),
+                                  tokens.data_ptr(), _ptr(committed_now), _ptr(conf), _ptr(n_masked),
+                                  ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+            "tt_block_step")
+
+
+def tt_get_device_error(dev_err: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream and return the device error word (0 = no error)."""
+    code = ctypes.c_uint32(0)
+    N.check(N.lib().tt_get_device_error(dev_err.data_ptr(), _stream(stream), ctypes.byref(code)),
+            "tt_get_device_error")
+    return int(code.value)

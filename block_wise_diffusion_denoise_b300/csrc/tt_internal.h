@@ -1,0 +1,55 @@
+// Internal launchers shared by the C-ABI layer and the kernel files (host side).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tt_denoise.h"
+
+namespace tt {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- unmasking
+struct UnmaskPartial {   // one (row, chunk) of the vocabulary
+    float m;             // chunk maximum
+    float z;             // sum of exp(x - m) over the chunk
+    int32_t arg;         // lowest index of the maximum
+    int32_t pad;
+};
+
+int unmask_chunk_elems(tt_dtype dtype);
+size_t unmask_ws_bytes(int B, int S, int V, tt_dtype dtype);
+tt_status launch_unmask(const void *logits, tt_dtype dtype, int B, int S, int V, float tau,
+                        int step, int T, uint8_t *masked, int32_t *tokens, uint8_t *committed_now,
+                        float *conf, int32_t *n_masked, void *ws, uint32_t *dev_err,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------- append
+tt_status launch_kv_append(const tt_kv_cache *layers, int n_layers, const void *const *k_new,
+                           const void *const *v_new, const uint8_t *seq_active, int B, int S,
+                           uint32_t *dev_err, cudaStream_t stream);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+    const tt_kv_cache *ctx;
+    const void *q, *k_blk, *v_blk;
+    void *out;
+    float *lse;
+    int B, S, Hq, Hkv, D;
+    float sm_scale;
+    int max_ctas;
+    void *ws;
+    size_t ws_bytes;
+    uint32_t *dev_err;
+    cudaStream_t stream;
+};
+
+tt_status launch_attn_simt(const AttnArgs &a);
+
+bool attn_tc_supported(int S, int Hq, int Hkv, int D, int page_size, tt_dtype dtype);
+size_t attn_tc_ws_bytes(int B, int S, int Hq, int Hkv, int D);
+tt_status launch_attn_tc(const AttnArgs &a);
+
+}  // namespace tt

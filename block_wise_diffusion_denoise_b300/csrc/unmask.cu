@@ -1,0 +1,306 @@
+// Confidence unmasking of one denoise step (tt_unmask).
+//
+// Rule (TwoTower summary on gist.science, "Training und Konditionierung --
+// Sampling" and "Der Konfidenz-Trick"): every still-masked position of the
+// block is predicted in parallel; positions whose confidence (largest softmax
+// probability) reaches the threshold are committed and locked, the others stay
+// masked.  Completed by two rules that keep a block finite: if nothing reaches
+// the threshold the single most confident masked position is committed, and at
+// the last step every masked position is committed.
+//
+// Design: HBM-bound single pass over the masked rows' logits.  The grid is
+// (vocabulary chunk, position, sequence); each CTA streams one 32 KB chunk of
+// one row with 16-byte loads (all of a thread's loads are issued before any is
+// used), reduces max / first-argmax / sum of exp relative to the CTA maximum,
+// and writes one partial.  The last CTA of a sequence to finish (atomic ticket,
+// no waiting) merges the partials of the sequence's rows in a fixed order and
+// applies the commit rules.  Locked rows cost one byte read.
+
+#include <cfloat>
+#include <climits>
+
+#include "tt_common.cuh"
+#include "tt_internal.h"
+
+namespace tt {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kLoadsPerThread = 8;   // 16-byte loads in flight per thread
+
+struct UnmaskParams {
+    const void *logits;
+    int B, S, V, nchunk;
+    float tau;
+    int step, T;
+    uint8_t *masked;
+    int32_t *tokens;
+    uint8_t *committed_now;
+    float *conf;
+    int32_t *n_masked;
+    UnmaskPartial *part;
+    unsigned *tickets;
+    uint32_t *dev_err;
+};
+
+template <typename T> struct Vec;
+template <> struct Vec<uint16_t> { static constexpr int kElems = 8; };
+template <> struct Vec<float> { static constexpr int kElems = 4; };
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4 &u, float *x);
+template <>
+__device__ __forceinline__ void unpack<uint16_t>(const uint4 &u, float *x) {
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
+    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
+    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4 &u, float *x) {
+    x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+}
+
+template <typename T> __device__ __forceinline__ float load_scalar(const T *p);
+template <> __device__ __forceinline__ float load_scalar<uint16_t>(const uint16_t *p) {
+    return bf16_bits_to_f32(*p);
+}
+template <> __device__ __forceinline__ float load_scalar<float>(const float *p) { return *p; }
+
+__device__ __forceinline__ float block_max(float v, float *sm) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) sm[w] = v;
+    __syncthreads();
+    v = (l < kWarps) ? sm[l] : -INFINITY;
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    return v;
+}
+
+__device__ __forceinline__ int block_min(int v, int *sm) {
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) sm[w] = v;
+    __syncthreads();
+    v = (l < kWarps) ? sm[l] : INT_MAX;
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    return v;
+}
+
+// Deterministic: a fixed shuffle tree per warp, then the warps in order.
+__device__ __forceinline__ float block_sum(float v, float *sm) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) sm[w] = v;
+    __syncthreads();
+    v = (l < kWarps) ? sm[l] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    return v;
+}
+
+// Merge two (max, sum-exp relative to max, first argmax) triples.
+__device__ __forceinline__ void merge(float &m, float &z, int &a, float m2, float z2, int a2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) { m = m2; z = z2; a = a2; return; }
+    const float M = fmaxf(m, m2);
+    z = z * fast_exp2((m - M) * kLog2e) + z2 * fast_exp2((m2 - M) * kLog2e);
+    a = (m > m2) ? a : (m2 > m) ? a2 : min(a, a2);
+    m = M;
+}
+
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) {
+    constexpr int EPV = Vec<T>::kElems;               // elements per 16-byte load
+    constexpr int NX = kLoadsPerThread * EPV;         // elements per thread
+    constexpr int CE = kThreads * NX;                 // elements per chunk
+    __shared__ float s_f[kWarps];
+    __shared__ int s_i[kWarps];
+    __shared__ int s_last;
+
+    const int chunk = blockIdx.x, pos = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x;
+    const size_t row = (size_t)b * p.S + pos;
+    const T *rowp = static_cast<const T *>(p.logits) + row * (size_t)p.V;
+
+    if (p.masked[row] != 0) {
+        const int c0 = chunk * CE;
+        float x[NX];
+        if constexpr (kVec) {
+            uint4 u[kLoadsPerThread];
+#pragma unroll
+            for (int i = 0; i < kLoadsPerThread; ++i) {
+                const int e = c0 + (i * kThreads + tid) * EPV;
+                u[i] = (e < p.V) ? ld_nc_v4(rowp + e) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < kLoadsPerThread; ++i) {
+                const int e = c0 + (i * kThreads + tid) * EPV;
+                unpack<T>(u[i], x + i * EPV);
+                if (e >= p.V) {
+#pragma unroll
+                    for (int j = 0; j < EPV; ++j) x[i * EPV + j] = -INFINITY;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kLoadsPerThread; ++i) {
+#pragma unroll
+                for (int j = 0; j < EPV; ++j) {
+                    const int e = c0 + (i * kThreads + tid) * EPV + j;
+                    x[i * EPV + j] = (e < p.V) ? load_scalar<T>(rowp + e) : -INFINITY;
+                }
+            }
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NX; ++k) mt = fmaxf(mt, x[k]);
+        const float M = block_max(mt, s_f);
+        // Lowest index holding the chunk maximum: only threads that hold it search,
+        // in increasing index order.
+        int at = INT_MAX;
+        if (mt == M) {
+#pragma unroll
+            for (int i = kLoadsPerThread - 1; i >= 0; --i) {
+#pragma unroll
+                for (int j = EPV - 1; j >= 0; --j) {
+                    if (x[i * EPV + j] == M) at = c0 + (i * kThreads + tid) * EPV + j;
+                }
+            }
+        }
+        const int A = block_min(at, s_i);
+        float z = 0.f;
+        const float mc = M * kLog2e;
+#pragma unroll
+        for (int k = 0; k < NX; ++k) z += fast_exp2(fmaf(x[k], kLog2e, -mc));
+        const float Z = block_sum(z, s_f);
+        if (tid == 0) {
+            UnmaskPartial q;
+            q.m = M; q.z = Z; q.arg = A; q.pad = 0;
+            p.part[row * p.nchunk + chunk] = q;
+        }
+    }
+
+    // Ticket: the last CTA of this sequence applies the commit rules.
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const unsigned t = atomicAdd(&p.tickets[b], 1u);
+        s_last = (t == (unsigned)(p.S * p.nchunk - 1));
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    extern __shared__ unsigned char dyn[];
+    float *s_conf = reinterpret_cast<float *>(dyn);
+    int *s_arg = reinterpret_cast<int *>(s_conf + p.S);
+    int *s_commit = s_arg + p.S;
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int r = warp; r < p.S; r += kWarps) {
+        const size_t rr = (size_t)b * p.S + r;
+        if (p.masked[rr] == 0) {
+            if (lane == 0) { s_conf[r] = NAN; s_arg[r] = -1; }
+            continue;
+        }
+        float m = -INFINITY, zz = 0.f;
+        int a = INT_MAX;
+        for (int c = lane; c < p.nchunk; c += 32) {
+            const UnmaskPartial *qp = p.part + rr * p.nchunk + c;
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(qp));
+            merge(m, zz, a, v.x, v.y, __float_as_int(v.z));
+        }
+        for (int o = 1; o < 32; o <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float z2 = __shfl_xor_sync(0xffffffffu, zz, o);
+            const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+            // both lanes of a pair merge in the same (lower lane first) order
+            if (lane & o) { float tm = m, tz = zz; int ta = a; m = m2; zz = z2; a = a2; merge(m, zz, a, tm, tz, ta); }
+            else merge(m, zz, a, m2, z2, a2);
+        }
+        if (lane == 0) { s_conf[r] = 1.0f / zz; s_arg[r] = a; }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const bool last_step = p.step >= p.T;
+        int n_commit = 0, best = -1;
+        float best_conf = -1.f;
+        for (int r = 0; r < p.S; ++r) {
+            const bool m = p.masked[(size_t)b * p.S + r] != 0;
+            const bool c = m && (last_step || s_conf[r] >= p.tau);
+            s_commit[r] = c;
+            n_commit += c;
+            if (m && s_conf[r] > best_conf) { best_conf = s_conf[r]; best = r; }
+        }
+        if (n_commit == 0 && best >= 0) s_commit[best] = 1;
+    }
+    __syncthreads();
+    int left = 0;
+    for (int r = tid; r < p.S; r += kThreads) {
+        const size_t rr = (size_t)b * p.S + r;
+        const bool m = p.masked[rr] != 0;
+        const bool c = s_commit[r] != 0;
+        if (c) { p.tokens[rr] = s_arg[r]; p.masked[rr] = 0; }
+        if (p.committed_now) p.committed_now[rr] = c ? 1 : 0;
+        if (p.conf) p.conf[rr] = s_conf[r];
+        left += (m && !c) ? 1 : 0;
+    }
+    // count of positions left masked
+    for (int o = 16; o > 0; o >>= 1) left += __shfl_xor_sync(0xffffffffu, left, o);
+    __syncthreads();
+    if (lane == 0) s_i[warp] = left;
+    __syncthreads();
+    if (tid == 0) {
+        int tot = 0;
+        for (int w = 0; w < kWarps; ++w) tot += s_i[w];
+        if (p.n_masked) p.n_masked[b] = tot;
+        p.tickets[b] = 0;   // leave the workspace ready for the next call
+    }
+}
+
+}  // namespace
+
+int unmask_chunk_elems(tt_dtype dtype) {
+    return kThreads * kLoadsPerThread * (dtype == TT_BF16 ? 8 : 4);
+}
+
+size_t unmask_ws_bytes(int B, int S, int V, tt_dtype dtype) {
+    const size_t nchunk = (size_t)((V + unmask_chunk_elems(dtype) - 1) / unmask_chunk_elems(dtype));
+    return align_up((size_t)B * S * nchunk * sizeof(UnmaskPartial), 256) +
+           align_up((size_t)B * sizeof(unsigned), 256);
+}
+
+tt_status launch_unmask(const void *logits, tt_dtype dtype, int B, int S, int V, float tau,
+                        int step, int T, uint8_t *masked, int32_t *tokens, uint8_t *committed_now,
+                        float *conf, int32_t *n_masked, void *ws, uint32_t *dev_err,
+                        cudaStream_t stream) {
+    UnmaskParams p;
+    p.logits = logits;
+    p.B = B; p.S = S; p.V = V;
+    p.nchunk = (V + unmask_chunk_elems(dtype) - 1) / unmask_chunk_elems(dtype);
+    p.tau = tau; p.step = step; p.T = T;
+    p.masked = masked; p.tokens = tokens; p.committed_now = committed_now; p.conf = conf;
+    p.n_masked = n_masked;
+    p.part = static_cast<UnmaskPartial *>(ws);
+    p.tickets = reinterpret_cast<unsigned *>(
+        static_cast<char *>(ws) + align_up((size_t)B * S * p.nchunk * sizeof(UnmaskPartial), 256));
+    p.dev_err = dev_err;
+    const dim3 grid(p.nchunk, S, B);
+    const size_t smem = (size_t)S * 3 * sizeof(float);
+    const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
+                     (V % (dtype == TT_BF16 ? 8 : 4) == 0);
+    if (dtype == TT_BF16) {
+        if (vec) unmask_kernel<uint16_t, true><<<grid, kThreads, smem, stream>>>(p);
+        else unmask_kernel<uint16_t, false><<<grid, kThreads, smem, stream>>>(p);
+    } else {
+        if (vec) unmask_kernel<float, true><<<grid, kThreads, smem, stream>>>(p);
+        else unmask_kernel<float, false><<<grid, kThreads, smem, stream>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+}  // namespace tt

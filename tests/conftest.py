@@ -11,3 +11,10 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
     config.addinivalue_line("markers", "slow: large CPU work")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def native_library():
+    """Build libtt_denoise.so in-tree if it is missing or older than its sources."""
+    from block_wise_diffusion_denoise_b300 import build
+    return build.build()

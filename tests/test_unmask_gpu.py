@@ -1,0 +1,123 @@
+"""Confidence unmasking on the GPU (tt_unmask) against the float64 oracle: commit masks
+and token ids bit-exact outside the near-threshold band, confidences to 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_wise_diffusion_denoise_b300 import api, synth
+from tests import support
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_step(logits_bits, dtype, masked, tokens, tau, step, T, ws=None):
+    B, S, V = logits_bits.shape
+    lg = support.to_dev(logits_bits, dtype)
+    m = torch.from_numpy(masked.astype(np.uint8)).cuda()
+    t = torch.from_numpy(tokens.astype(np.int32)).cuda()
+    com = torch.full((B, S), 7, dtype=torch.uint8, device="cuda")
+    conf = torch.zeros((B, S), dtype=torch.float32, device="cuda")
+    nm = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    err = api.error_word()
+    api.tt_unmask(lg, m, t, tau, step, T, committed_now=com, conf=conf, n_masked=nm, ws=ws, dev_err=err)
+    assert api.tt_get_device_error(err) == 0
+    return (m.cpu().numpy(), t.cpu().numpy(), com.cpu().numpy(), conf.cpu().numpy(), nm.cpu().numpy())
+
+
+def _check_step(logits_bits, dtype, masked, tokens, tau, step, T, ws=None):
+    g = _run_step(logits_bits, dtype, masked, tokens, tau, step, T, ws)
+    ora = oracle.unmask(logits_bits, masked, tokens, tau, step, T, dtype)
+    ex = support.compare_unmask(masked, tokens, ora, *g, tau, step, T)
+    return g, ora, ex
+
+
+def test_tiny_fp32_block_loop():
+    cfg = synth.CONFIGS["tiny"]
+    ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.float32))
+    for blk in range(6):
+        masked = np.ones((cfg.B, cfg.S), np.uint8)
+        tokens = np.full((cfg.B, cfg.S), -1, np.int32)
+        for step in range(1, cfg.T + 1):
+            lg = synth.draw_logits(cfg, seed=blk, block=blk, step=step)
+            (m, t, com, conf, nm), ora, _ = _check_step(lg, "f32", masked, tokens, cfg.tau, step, cfg.T, ws)
+            assert com.sum() >= 1 or masked.sum() == 0
+            masked, tokens = m, t
+            if not masked.any():
+                break
+        assert not masked.any()        # every block finishes within T steps
+
+
+@pytest.mark.parametrize("peak_hi", [12.0, 40.0])
+def test_single_bf16_full_vocab(peak_hi):
+    cfg = synth.CONFIGS["single"]
+    lg = synth.draw_logits(cfg, seed=3, peak_hi=peak_hi)
+    masked = np.ones((cfg.B, cfg.S), np.uint8)
+    tokens = np.full((cfg.B, cfg.S), -1, np.int32)
+    for step in (1, cfg.T):
+        _check_step(lg, "bf16", masked, tokens, cfg.tau, step, cfg.T)
+
+
+def test_batch_sharp_variant_every_branch():
+    """B=32, V=131072; peaks U[0,40] so that the threshold, the fallback and step T all occur."""
+    cfg = synth.CONFIGS["ctx8k"]
+    rng = np.random.default_rng(11)
+    ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.bfloat16))
+    lg = synth.draw_logits(cfg, seed=5, peak_hi=40.0)
+    masked = (rng.random((cfg.B, cfg.S)) < 0.8).astype(np.uint8)
+    masked[:, 0] = 1
+    tokens = np.where(masked == 1, -1, rng.integers(0, cfg.V, (cfg.B, cfg.S))).astype(np.int32)
+    saw_thr = saw_fb = False
+    for step in (1, 7, cfg.T):
+        (m, t, com, conf, nm), ora, _ = _check_step(lg, "bf16", masked, tokens, cfg.tau, step, cfg.T, ws)
+        if step < cfg.T:
+            saw_fb |= any(r.fallback for r in ora)
+            saw_thr |= any((r.committed_now.sum() > 0 and not r.fallback) for r in ora)
+    assert saw_thr and saw_fb
+
+
+def test_locked_rows_are_never_read_and_ties_take_lowest_id():
+    cfg = synth.CONFIGS["single"].replace(B=3, V=40000)
+    lg = synth.draw_logits(cfg, seed=9, peak_hi=30.0)
+    vals = oracle.decode(lg, "bf16")
+    # exact ties at the maximum: copy the row maximum to a later and an earlier index
+    for b in range(cfg.B):
+        for p in range(0, cfg.S, 3):
+            a = int(np.argmax(vals[b, p]))
+            lg[b, p, min(cfg.V - 1, a + 17)] = lg[b, p, a]
+            if a > 5:
+                lg[b, p, a - 5] = lg[b, p, a]
+    masked = np.ones((cfg.B, cfg.S), np.uint8)
+    masked[:, 1::4] = 0
+    tokens = np.where(masked == 1, -1, 123).astype(np.int32)
+    lg_nan = lg.copy()
+    lg_nan[masked == 0] = np.uint16(0x7FC0)          # NaN rows where positions are locked
+    for step in (1, 2, cfg.T):
+        g = _run_step(lg_nan, "bf16", masked, tokens, cfg.tau, step, cfg.T)
+        ora = oracle.unmask(lg, masked, tokens, cfg.tau, step, cfg.T, "bf16")
+        support.compare_unmask(masked, tokens, ora, *g, cfg.tau, step, cfg.T)
+
+
+@pytest.mark.parametrize("V", [1, 7, 1003, 16384, 16385, 50001])
+def test_ragged_vocab_sizes(V):
+    """Vocabulary sizes that are not a multiple of the vector width or of the chunk."""
+    for dtype in ("bf16", "f32"):
+        cfg = synth.CONFIGS["tiny"].replace(B=2, V=V, dtype=dtype)
+        lg = synth.draw_logits(cfg, seed=V, peak_hi=20.0)
+        masked = np.ones((cfg.B, cfg.S), np.uint8)
+        tokens = np.full((cfg.B, cfg.S), -1, np.int32)
+        for step in (1, cfg.T):
+            _check_step(lg, dtype, masked, tokens, cfg.tau, step, cfg.T)
+
+
+def test_nothing_masked_and_empty_batch():
+    cfg = synth.CONFIGS["tiny"].replace(B=2)
+    lg = synth.draw_logits(cfg, seed=1)
+    masked = np.zeros((cfg.B, cfg.S), np.uint8)
+    tokens = np.arange(cfg.B * cfg.S, dtype=np.int32).reshape(cfg.B, cfg.S)
+    m, t, com, conf, nm = _run_step(lg, "f32", masked, tokens, 0.9, 1, 4)
+    assert not com.any() and np.array_equal(t, tokens) and (nm == 0).all() and np.isnan(conf).all()
+    empty = torch.zeros((0, 16, 64), dtype=torch.float32, device="cuda")
+    api.tt_unmask(empty, torch.zeros((0, 16), dtype=torch.uint8, device="cuda"),
+                  torch.zeros((0, 16), dtype=torch.int32, device="cuda"), 0.9, 1, 4)
+    torch.cuda.synchronize()
