@@ -72,28 +72,34 @@ def unmask_bytes(cfg, masked_rows) -> float:
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """Polls NVML for the SM clock and throttle reasons from a thread while the timed region runs."""
+    """Samples the SM clock and throttle reasons while the timed region runs: NVML from a
+    thread when the Python bindings are present, otherwise an ``nvidia-smi -lms`` child."""
     REASONS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
                "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
-        self.samples, self.reasons, self.ok = [], set(), False
+        import torch
+        self.samples, self.reasons, self.mode, self.max_mhz = [], set(), None, None
         self._stop = threading.Event()
+        pr = torch.cuda.get_device_properties(index)
+        self.bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
         try:
             import pynvml
-            import torch
             pynvml.nvmlInit()
             self.nv = pynvml
-            pr = torch.cuda.get_device_properties(index)
-            try:   # match the CUDA device to its NVML handle by PCI address
-                bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
-                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            try:
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus)
             except Exception:
                 self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # NVML absent: report it instead of a clock
-            self.err = repr(e)
+            self.mode = "nvml"
+        except Exception:
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "smi"
 
     def _run(self):
         while not self._stop.is_set():
@@ -108,21 +114,42 @@ class ClockSampler:
             time.sleep(0.002)
 
     def __enter__(self):
-        if self.ok:
+        if self.mode == "nvml":
             self.t = threading.Thread(target=self._run, daemon=True)
             self.t.start()
+        elif self.mode == "smi":
+            import subprocess
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.bus, f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)          # let the first sample land before the timed region
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif self.mode == "smi":
+            time.sleep(0.05)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6 or not f[0].isdigit():
+                    continue
+                self.samples.append(int(f[0]))
+                self.max_mhz = int(f[1]) if f[1].isdigit() else self.max_mhz
+                for name, val in zip(names, f[2:6]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": getattr(self, "err", "")}
+        if self.mode is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": "no NVML and no nvidia-smi"}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": self.mode}
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
@@ -355,7 +382,7 @@ def run_ours(a, cfg):
         tokens[a.warmup:].fill_(-1)
         barrier()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with sampler:
+        with sampler, torch.cuda.stream(s):
             ev0.record(s)
             g.replay()
             ev1.record(s)

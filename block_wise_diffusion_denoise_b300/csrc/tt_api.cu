@@ -84,7 +84,7 @@ tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const void *k_b
     a.B = B; a.S = S; a.Hq = Hq; a.Hkv = ctx->n_kv_heads; a.D = ctx->head_dim;
     a.sm_scale = sm_scale; a.max_ctas = max_ctas; a.ws = ws; a.ws_bytes = ws_bytes;
     a.dev_err = dev_err; a.stream = reinterpret_cast<cudaStream_t>(stream);
-    if (attn_tc_supported(S, Hq, a.Hkv, a.D, ctx->page_size, (tt_dtype)ctx->dtype)) {
+    if (attn_tc_supported(S, Hq, a.Hkv, a.D, ctx->page_size, (tt_dtype)ctx->dtype) && sm_scale > 0.f) {
         const size_t need = attn_tc_ws_bytes(B, S, Hq, a.Hkv, a.D);
         if (need > 0 && (ws == nullptr || ws_bytes < need)) return TT_ERR_CAPACITY;
         if (need > 0 && reinterpret_cast<uintptr_t>(ws) % 256 != 0) return TT_ERR_UNSUPPORTED;

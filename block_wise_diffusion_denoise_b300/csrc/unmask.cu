@@ -9,25 +9,31 @@
 // the last step every masked position is committed.
 //
 // Design: HBM-bound single pass over the masked rows' logits.  The grid is
-// (vocabulary chunk, position, sequence); each CTA streams one 32 KB chunk of
-// one row with 16-byte loads (all of a thread's loads are issued before any is
-// used), reduces max / first-argmax / sum of exp relative to the CTA maximum,
-// and writes one partial.  The last CTA of a sequence to finish (atomic ticket,
-// no waiting) merges the partials of the sequence's rows in a fixed order and
-// applies the commit rules.  Locked rows cost one byte read.
+// (vocabulary chunk, position, sequence); each CTA brings one 32 KB chunk of one
+// row into shared memory with four bulk copies (cp.async.bulk, one mbarrier per
+// 8 KB piece) issued before any arithmetic, so up to six CTAs per SM keep about
+// 190 KB in flight with few registers.  Threads fold each piece into an online
+// (max, sum of exp relative to the max, first argmax) state, the CTA merges the
+// states in a fixed order and writes one partial.  The last CTA of a sequence to
+// finish (atomic ticket, no waiting) merges the partials of the sequence's rows
+// and applies the commit rules.  Locked rows cost one byte read.
 
 #include <cfloat>
 #include <climits>
 
+#include "sm100_ptx.cuh"
 #include "tt_common.cuh"
 #include "tt_internal.h"
 
 namespace tt {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLoadsPerThread = 8;   // 16-byte loads in flight per thread
+constexpr int kChunkBytes = 32768;   // one CTA's share of a row
+constexpr int kPieces = 4;           // bulk copies (and mbarriers) per chunk
+constexpr int kPieceBytes = kChunkBytes / kPieces;
+constexpr uint32_t kWaitLimit = 1u << 24;
 
 struct UnmaskParams {
     const void *logits;
@@ -69,40 +75,6 @@ template <> __device__ __forceinline__ float load_scalar<uint16_t>(const uint16_
 }
 template <> __device__ __forceinline__ float load_scalar<float>(const float *p) { return *p; }
 
-__device__ __forceinline__ float block_max(float v, float *sm) {
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) sm[w] = v;
-    __syncthreads();
-    v = (l < kWarps) ? sm[l] : -INFINITY;
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    return v;
-}
-
-__device__ __forceinline__ int block_min(int v, int *sm) {
-    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) sm[w] = v;
-    __syncthreads();
-    v = (l < kWarps) ? sm[l] : INT_MAX;
-    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    return v;
-}
-
-// Deterministic: a fixed shuffle tree per warp, then the warps in order.
-__device__ __forceinline__ float block_sum(float v, float *sm) {
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) sm[w] = v;
-    __syncthreads();
-    v = (l < kWarps) ? sm[l] : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    return v;
-}
-
 // Merge two (max, sum-exp relative to max, first argmax) triples.
 __device__ __forceinline__ void merge(float &m, float &z, int &a, float m2, float z2, int a2) {
     if (m2 == -INFINITY) return;
@@ -113,13 +85,54 @@ __device__ __forceinline__ void merge(float &m, float &z, int &a, float m2, floa
     m = M;
 }
 
+// Warp-wide merge; both lanes of every pair merge (lower lane, upper lane) in that
+// order, so all lanes end with the same, order-fixed result.
+__device__ __forceinline__ void warp_merge(float &m, float &z, int &a) {
+    const int lane = threadIdx.x & 31;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+        const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane & o) {
+            const float tm = m, tz = z;
+            const int ta = a;
+            m = m2; z = z2; a = a2;
+            merge(m, z, a, tm, tz, ta);
+        } else {
+            merge(m, z, a, m2, z2, a2);
+        }
+    }
+}
+
+// Fold EPV consecutive elements starting at index e0 into the running state.
+// A new maximum must be strictly larger, so the first index of a repeated
+// maximum is kept.
+template <int EPV>
+__device__ __forceinline__ void fold(const float *x, int e0, float &m, float &z, int &a) {
+    float gm = x[0];
+#pragma unroll
+    for (int j = 1; j < EPV; ++j) gm = fmaxf(gm, x[j]);
+    if (gm > m) {
+        z = (m == -INFINITY) ? 0.f : z * fast_exp2((m - gm) * kLog2e);
+        m = gm;
+        int j0 = EPV - 1;
+#pragma unroll
+        for (int j = EPV - 1; j >= 0; --j) j0 = (x[j] == gm) ? j : j0;
+        a = e0 + j0;
+    }
+    const float mc = m * kLog2e;
+#pragma unroll
+    for (int j = 0; j < EPV; ++j) z += fast_exp2(fmaf(x[j], kLog2e, -mc));
+}
+
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) {
-    constexpr int EPV = Vec<T>::kElems;               // elements per 16-byte load
-    constexpr int NX = kLoadsPerThread * EPV;         // elements per thread
-    constexpr int CE = kThreads * NX;                 // elements per chunk
-    __shared__ float s_f[kWarps];
-    __shared__ int s_i[kWarps];
+    constexpr int EPV = Vec<T>::kElems;               // elements per 16-byte vector
+    constexpr int CE = kChunkBytes / (int)sizeof(T);  // elements per chunk
+    __shared__ __align__(128) uint4 buf[kVec ? kChunkBytes / 16 : 1];
+    __shared__ uint64_t bars[kPieces];
+    __shared__ float s_m[kWarps], s_z[kWarps];
+    __shared__ int s_a[kWarps];
     __shared__ int s_last;
 
     const int chunk = blockIdx.x, pos = blockIdx.y, b = blockIdx.z;
@@ -129,56 +142,60 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) 
 
     if (p.masked[row] != 0) {
         const int c0 = chunk * CE;
-        float x[NX];
+        const int n = min(CE, p.V - c0);                 // elements of this chunk
+        float m = -INFINITY, z = 0.f;
+        int a = INT_MAX;
         if constexpr (kVec) {
-            uint4 u[kLoadsPerThread];
-#pragma unroll
-            for (int i = 0; i < kLoadsPerThread; ++i) {
-                const int e = c0 + (i * kThreads + tid) * EPV;
-                u[i] = (e < p.V) ? ld_nc_v4(rowp + e) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int i = 0; i < kLoadsPerThread; ++i) {
-                const int e = c0 + (i * kThreads + tid) * EPV;
-                unpack<T>(u[i], x + i * EPV);
-                if (e >= p.V) {
-#pragma unroll
-                    for (int j = 0; j < EPV; ++j) x[i * EPV + j] = -INFINITY;
+            const int bytes = n * (int)sizeof(T);        // a multiple of 16 on this path
+            if (tid == 0) {
+                for (int k = 0; k < kPieces; ++k) sm100::mbar_init(&bars[k], 1);
+                sm100::fence_mbar_init();
+                for (int k = 0; k < kPieces; ++k) {
+                    const int pb = min(kPieceBytes, bytes - k * kPieceBytes);
+                    if (pb <= 0) break;
+                    sm100::mbar_arrive_expect_tx(&bars[k], (uint32_t)pb);
+                    sm100::bulk_load(reinterpret_cast<char *>(buf) + k * kPieceBytes,
+                                     reinterpret_cast<const char *>(rowp + c0) + k * kPieceBytes, (uint32_t)pb,
+                                     &bars[k]);
                 }
+            }
+            __syncthreads();
+            bool timed_out = false;
+            for (int k = 0; k < kPieces; ++k) {
+                const int pb = min(kPieceBytes, bytes - k * kPieceBytes);
+                if (pb <= 0) break;
+                if (!sm100::mbar_wait(&bars[k], 0, kWaitLimit)) {
+                    timed_out = true;
+                    break;
+                }
+                const int nv = pb / 16;
+                const uint4 *pv = buf + k * (kPieceBytes / 16);
+                for (int v = tid; v < nv; v += kThreads) {
+                    float x[EPV];
+                    unpack<T>(pv[v], x);
+                    fold<EPV>(x, c0 + (k * (kPieceBytes / 16) + v) * EPV, m, z, a);
+                }
+            }
+            if (timed_out) {
+                if (tid == 0) report_error(p.dev_err, TT_ERR_DEVICE_TIMEOUT);
+                // give the copies a second bounded chance to land before the CTA leaves
+                for (int k = 0; k < kPieces; ++k)
+                    if (min(kPieceBytes, bytes - k * kPieceBytes) > 0) sm100::mbar_wait(&bars[k], 0, kWaitLimit);
             }
         } else {
-#pragma unroll
-            for (int i = 0; i < kLoadsPerThread; ++i) {
-#pragma unroll
-                for (int j = 0; j < EPV; ++j) {
-                    const int e = c0 + (i * kThreads + tid) * EPV + j;
-                    x[i * EPV + j] = (e < p.V) ? load_scalar<T>(rowp + e) : -INFINITY;
-                }
+            for (int e = tid; e < n; e += kThreads) {
+                const float x = load_scalar<T>(rowp + c0 + e);
+                fold<1>(&x, c0 + e, m, z, a);
             }
         }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < NX; ++k) mt = fmaxf(mt, x[k]);
-        const float M = block_max(mt, s_f);
-        // Lowest index holding the chunk maximum: only threads that hold it search,
-        // in increasing index order.
-        int at = INT_MAX;
-        if (mt == M) {
-#pragma unroll
-            for (int i = kLoadsPerThread - 1; i >= 0; --i) {
-#pragma unroll
-                for (int j = EPV - 1; j >= 0; --j) {
-                    if (x[i * EPV + j] == M) at = c0 + (i * kThreads + tid) * EPV + j;
-                }
-            }
-        }
-        const int A = block_min(at, s_i);
-        float z = 0.f;
-        const float mc = M * kLog2e;
-#pragma unroll
-        for (int k = 0; k < NX; ++k) z += fast_exp2(fmaf(x[k], kLog2e, -mc));
-        const float Z = block_sum(z, s_f);
+        warp_merge(m, z, a);
+        const int w = tid >> 5;
+        if ((tid & 31) == 0) { s_m[w] = m; s_z[w] = z; s_a[w] = a; }
+        __syncthreads();
         if (tid == 0) {
+            float M = s_m[0], Z = s_z[0];
+            int A = s_a[0];
+            for (int k = 1; k < kWarps; ++k) merge(M, Z, A, s_m[k], s_z[k], s_a[k]);
             UnmaskPartial q;
             q.m = M; q.z = Z; q.arg = A; q.pad = 0;
             p.part[row * p.nchunk + chunk] = q;
@@ -214,14 +231,7 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) 
             const float4 v = __ldcg(reinterpret_cast<const float4 *>(qp));
             merge(m, zz, a, v.x, v.y, __float_as_int(v.z));
         }
-        for (int o = 1; o < 32; o <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float z2 = __shfl_xor_sync(0xffffffffu, zz, o);
-            const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
-            // both lanes of a pair merge in the same (lower lane first) order
-            if (lane & o) { float tm = m, tz = zz; int ta = a; m = m2; zz = z2; a = a2; merge(m, zz, a, tm, tz, ta); }
-            else merge(m, zz, a, m2, z2, a2);
-        }
+        warp_merge(m, zz, a);
         if (lane == 0) { s_conf[r] = 1.0f / zz; s_arg[r] = a; }
     }
     __syncthreads();
@@ -252,11 +262,11 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) 
     // count of positions left masked
     for (int o = 16; o > 0; o >>= 1) left += __shfl_xor_sync(0xffffffffu, left, o);
     __syncthreads();
-    if (lane == 0) s_i[warp] = left;
+    if (lane == 0) s_a[warp] = left;
     __syncthreads();
     if (tid == 0) {
         int tot = 0;
-        for (int w = 0; w < kWarps; ++w) tot += s_i[w];
+        for (int w = 0; w < kWarps; ++w) tot += s_a[w];
         if (p.n_masked) p.n_masked[b] = tot;
         p.tickets[b] = 0;   // leave the workspace ready for the next call
     }
@@ -264,9 +274,7 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) 
 
 }  // namespace
 
-int unmask_chunk_elems(tt_dtype dtype) {
-    return kThreads * kLoadsPerThread * (dtype == TT_BF16 ? 8 : 4);
-}
+int unmask_chunk_elems(tt_dtype dtype) { return kChunkBytes / (dtype == TT_BF16 ? 2 : 4); }
 
 size_t unmask_ws_bytes(int B, int S, int V, tt_dtype dtype) {
     const size_t nchunk = (size_t)((V + unmask_chunk_elems(dtype) - 1) / unmask_chunk_elems(dtype));

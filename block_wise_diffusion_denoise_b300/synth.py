@@ -184,7 +184,7 @@ def draw_paged_cache(cfg: StepConfig, lens: np.ndarray, capacity_tokens: int, se
                 if rem:
                     live[page_table[b, full], :rem] = True
             fill = np.float32(np.nan) if garbage == "nan" else np.float32(3.0e38)
-            x[~live] = fill
+            x[np.broadcast_to((~live)[:, None, :, None], x.shape)] = fill
         pools.append(_encode(x, cfg.dtype))
     return PagedCache(pools[0], pools[1], page_table.astype(np.int32), lens.astype(np.int32).copy(),
                       cfg.page_size, cfg.dtype)

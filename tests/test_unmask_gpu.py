@@ -59,11 +59,13 @@ def test_single_bf16_full_vocab(peak_hi):
 
 
 def test_batch_sharp_variant_every_branch():
-    """B=32, V=131072; peaks U[0,40] so that the threshold, the fallback and step T all occur."""
+    """B=32, V=131072; peaks U[0,40] in half the sequences and U[0,12] in the other half, so that
+    the threshold, the fallback and step T all occur."""
     cfg = synth.CONFIGS["ctx8k"]
     rng = np.random.default_rng(11)
     ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.bfloat16))
     lg = synth.draw_logits(cfg, seed=5, peak_hi=40.0)
+    lg[cfg.B // 2:] = synth.draw_logits(cfg, seed=6, peak_hi=12.0)[cfg.B // 2:]   # mild half: fallback
     masked = (rng.random((cfg.B, cfg.S)) < 0.8).astype(np.uint8)
     masked[:, 0] = 1
     tokens = np.where(masked == 1, -1, rng.integers(0, cfg.V, (cfg.B, cfg.S))).astype(np.int32)
