@@ -7,4 +7,5 @@ draws seeded synthetic inputs.  Build the library with
 """
 from .api import (KVCache, TTError, error_word, tt_block_step, tt_block_step_workspace_size,  # noqa: F401
                   tt_denoise_attn, tt_denoise_attn_workspace_size, tt_get_device_error, tt_kv_append,
-                  tt_unmask, tt_unmask_workspace_size, workspace)
+                  tt_unmask, tt_unmask_noalloc, tt_unmask_workspace_size,
+                  workspace)

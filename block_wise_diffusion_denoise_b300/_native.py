@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtt_denoi
 TT_OK, TT_ERR_INVALID_ARG, TT_ERR_UNSUPPORTED, TT_ERR_CAPACITY, TT_ERR_CUDA, \
     TT_ERR_DEVICE_TIMEOUT, TT_ERR_BOUNDS = range(7)
 TT_BF16, TT_FP32 = 0, 1
+UNMASK_NOALLOC_SCRATCH_BYTES = 256 * 1024   # TT_UNMASK_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {
     TT_OK: "TT_OK", TT_ERR_INVALID_ARG: "TT_ERR_INVALID_ARG", TT_ERR_UNSUPPORTED: "TT_ERR_UNSUPPORTED",
@@ -23,8 +24,8 @@ STATUS_NAMES = {
 
 # Every symbol the header declares, in declaration order.
 EXPORTED = ("tt_status_string", "tt_version", "tt_denoise_attn_workspace_size", "tt_denoise_attn",
-            "tt_unmask_workspace_size", "tt_unmask", "tt_kv_append", "tt_block_step_workspace_size",
-            "tt_block_step", "tt_get_device_error")
+            "tt_unmask_workspace_size", "tt_unmask", "tt_unmask_noalloc", "tt_kv_append",
+            "tt_block_step_workspace_size", "tt_block_step", "tt_get_device_error")
 
 
 class NativeLibraryMissing(ImportError):
@@ -70,6 +71,7 @@ _SIGNATURES = {
                              _P, _P]),
     "tt_unmask_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
     "tt_unmask": (_I, [_P, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tt_unmask_noalloc": (_I, [_P, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "tt_kv_append": (_I, [ctypes.POINTER(tt_kv_cache), _I, _PP, _PP, _P, _I, _I, _P, _P]),
     "tt_block_step_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, _I, _PSZ]),
     "tt_block_step": (_I, [ctypes.POINTER(tt_kv_cache), _I, _PP, _PP, _PP, _PP, _P, _I, _I, _I, _I, _F, _I,

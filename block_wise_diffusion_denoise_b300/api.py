@@ -185,6 +185,29 @@ def tt_unmask(logits: torch.Tensor, masked: torch.Tensor, tokens: torch.Tensor, 
             "tt_unmask")
 
 
+def tt_unmask_noalloc(logits: torch.Tensor, masked: torch.Tensor, tokens: torch.Tensor, tau: float, step: int,
+                      T: int, committed_now: Optional[torch.Tensor] = None, conf: Optional[torch.Tensor] = None,
+                      n_masked: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """tt_unmask without a workspace, for callers that cannot allocate device memory (inside
+    graph capture, under a framework that owns the device pool, fixed-memory loops).  The
+    library's own file-scope scratch array is used instead; every call shares it, so calls
+    must not overlap on the GPU.  Make the first call on a device outside stream capture."""
+    B, S, V = logits.shape
+    if logits.dtype not in _DT:
+        raise ValueError("logits must be bf16 or fp32")
+    _need(logits, "logits")
+    _need(masked, "masked", torch.uint8, (B, S))
+    _need(tokens, "tokens", torch.int32, (B, S))
+    _need(committed_now, "committed_now", torch.uint8, (B, S), allow_none=True)
+    _need(conf, "conf", torch.float32, (B, S), allow_none=True)
+    _need(n_masked, "n_masked", torch.int32, (B,), allow_none=True)
+    N.check(N.lib().tt_unmask_noalloc(logits.data_ptr(), _DT[logits.dtype], B, S, V, float(tau), int(step),
+                                      int(T), masked.data_ptr(), tokens.data_ptr(), _ptr(committed_now),
+                                      _ptr(conf), _ptr(n_masked), _ptr(dev_err), _stream(stream)),
+            "tt_unmask_noalloc")
+
+
 def tt_kv_append(caches: Sequence[KVCache], k_new: Sequence[torch.Tensor], v_new: Sequence[torch.Tensor],
                  seq_active: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> None:

@@ -119,6 +119,19 @@ tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int V, flo
                          n_masked, ws, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tt_status tt_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S, int V, float tau, int step,
+                            int T, uint8_t *masked, int32_t *tokens, uint8_t *committed_now, float *conf,
+                            int32_t *n_masked, uint32_t *dev_err, tt_stream_t stream) {
+    if (B < 0 || S < 1 || V < 1 || !dtype_ok(dtype) || step < 1 || T < 1 || std::isnan(tau))
+        return TT_ERR_INVALID_ARG;
+    if (S > kMaxS) return TT_ERR_UNSUPPORTED;
+    if (B == 0) return TT_OK;
+    if (logits == nullptr || masked == nullptr || tokens == nullptr) return TT_ERR_INVALID_ARG;
+    if (B > 65535) return TT_ERR_UNSUPPORTED;
+    return launch_unmask_noalloc(logits, dtype, B, S, V, tau, step, T, masked, tokens, committed_now, conf,
+                                 n_masked, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 tt_status tt_kv_append(const tt_kv_cache *layers, int n_layers, const void *const *k_new,
                        const void *const *v_new, const uint8_t *seq_active, int B, int S,
                        uint32_t *dev_err, tt_stream_t stream) {

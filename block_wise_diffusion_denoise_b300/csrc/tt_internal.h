@@ -26,6 +26,11 @@ tt_status launch_unmask(const void *logits, tt_dtype dtype, int B, int S, int V,
                         float *conf, int32_t *n_masked, void *ws, uint32_t *dev_err,
                         cudaStream_t stream);
 
+tt_status launch_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S, int V, float tau,
+                                int step, int T, uint8_t *masked, int32_t *tokens,
+                                uint8_t *committed_now, float *conf, int32_t *n_masked,
+                                uint32_t *dev_err, cudaStream_t stream);
+
 // ---------------------------------------------------------------- append
 tt_status launch_kv_append(const tt_kv_cache *layers, int n_layers, const void *const *k_new,
                            const void *const *v_new, const uint8_t *seq_active, int B, int S,

@@ -20,6 +20,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "sm100_ptx.cuh"
 #include "tt_common.cuh"
@@ -309,6 +310,50 @@ tt_status launch_unmask(const void *logits, tt_dtype dtype, int B, int S, int V,
         else unmask_kernel<float, false><<<grid, kThreads, smem, stream>>>(p);
     }
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- scratch-free variant
+//
+// For callers that cannot allocate device memory (graph capture, pool-owning
+// frameworks, fixed-memory real-time loops): the same kernel, with its scratch in
+// this file-scope device array instead of a caller workspace.  The array is held
+// by every GPU that loads the library until the process exits; all calls share it.
+
+static __device__ __align__(256) unsigned char g_unmask_scratch[TT_UNMASK_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_scratch_once[kMaxDevices];
+void *g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+
+}  // namespace
+
+tt_status launch_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S, int V, float tau,
+                                int step, int T, uint8_t *masked, int32_t *tokens,
+                                uint8_t *committed_now, float *conf, int32_t *n_masked,
+                                uint32_t *dev_err, cudaStream_t stream) {
+    const size_t need = unmask_ws_bytes(B, S, V, dtype);
+    if (need > TT_UNMASK_NOALLOC_SCRATCH_BYTES) return TT_ERR_CAPACITY;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TT_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TT_ERR_UNSUPPORTED;
+    // Host code only holds a stand-in for the array; its device address comes from
+    // the runtime, once per device, with that device current.
+    std::call_once(g_scratch_once[dev], [dev] {
+        g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_unmask_scratch);
+    });
+    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return TT_ERR_CUDA;
+    void *ws = g_scratch_ptr[dev];
+    // The per-sequence counters must start at zero, whatever an earlier call left.
+    const int nchunk = (V + unmask_chunk_elems(dtype) - 1) / unmask_chunk_elems(dtype);
+    const size_t tick_off = align_up((size_t)B * S * nchunk * sizeof(UnmaskPartial), 256);
+    if (cudaMemsetAsync(static_cast<char *>(ws) + tick_off, 0, (size_t)B * sizeof(unsigned), stream) !=
+        cudaSuccess)
+        return TT_ERR_CUDA;
+    return launch_unmask(logits, dtype, B, S, V, tau, step, T, masked, tokens, committed_now, conf, n_masked,
+                         ws, dev_err, stream);
 }
 
 }  // namespace tt

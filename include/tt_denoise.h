@@ -184,6 +184,38 @@ TT_API tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int
                     int32_t *n_masked, void *ws, size_t ws_bytes, uint32_t *dev_err,
                     tt_stream_t stream);
 
+/* Largest scratch, in bytes, that tt_unmask_noalloc can use (its file-scope device array). */
+#define TT_UNMASK_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+
+/* tt_unmask for callers that cannot allocate device memory.  (The pages have no
+ * counterpart of this call; it exists for deployment.)
+ *
+ * Some callers cannot call cudaMalloc or any allocator: code that runs while a
+ * stream is being captured into a CUDA graph (allocation is not a capturable
+ * operation), plugins and callbacks inside a serving framework that owns every
+ * byte of device memory through its own pool, and real-time loops whose memory
+ * is fixed at start-up.  This call takes no workspace: its scratch (the
+ * per-chunk partials and the per-sequence counters) lives in one file-scope
+ * device array of TT_UNMASK_NOALLOC_SCRATCH_BYTES, which every GPU that loads
+ * the library holds until the process exits.  The caller still owns logits,
+ * masked, tokens and the outputs.  Arguments and results are exactly those of
+ * tt_unmask.
+ *
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - A shape whose scratch would exceed the array returns TT_ERR_CAPACITY before
+ *    anything is launched (tt_unmask_workspace_size gives the need; about 64 KB
+ *    for 32 sequences x 16 positions x 131072 bf16 logits).
+ *  - Every call shares the one array and it keeps the last call's contents; the
+ *    counters that must start at zero are cleared on the stream before each
+ *    launch.  Calls that overlap on the GPU (different streams, or several host
+ *    threads) race on the array and give wrong results: serialise them. */
+TT_API tt_status tt_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S, int V, float tau,
+                                   int step, int T, uint8_t *masked, int32_t *tokens,
+                                   uint8_t *committed_now, float *conf, int32_t *n_masked,
+                                   uint32_t *dev_err, tt_stream_t stream);
+
 /* Commit of a finished block into the context caches of n_layers layers ([GEN]:
  * the context tower extends its state with the clean tokens).
  *
