@@ -13,14 +13,18 @@
 //    the MMA: one or two 128-row tiles, each key tile is read from HBM once for
 //    all of them (256 flop per key byte at G*S = 256).
 //  * Tiles.  A key tile is one 64-token page of the paged cache (or the block's
-//    own S keys).  A dedicated producer thread moves K and V pages with TMA
-//    (128-byte swizzle) into a 3-stage shared-memory ring; Q of the segment is
-//    loaded once.  One thread issues tcgen05.mma: S = Q K^T into a
-//    double-buffered TMEM tile, then O += P V into TMEM accumulators.
+//    own S keys).  A producer warp moves K and V pages with TMA (128-byte
+//    swizzle) into separate rings (4 K stages, freed as soon as QK has read them;
+//    6 V stages, freed after PV), fetching page ids 32 at a time; Q of the
+//    segment is loaded once.  S = Q K^T goes to a double-buffered TMEM tile,
+//    then O += P V with P read from TMEM.  Each issuing thread waits about a
+//    hundred cycles per tcgen05.mma while the tensor pipe accepts several
+//    streams, so the QK product of each M tile and the PV product have their own
+//    issuing warps (one elected lane of a converged warp issues).
 //  * Softmax.  One thread per row (two warpgroups for two M tiles) reads its S
 //    row from TMEM, keeps the running maximum in the log2 domain and only
-//    rescales O (in TMEM) when the maximum grows by more than 2^8, writes P as
-//    bf16 into shared memory in the swizzled K-major layout the MMA reads.
+//    rescales O (in TMEM) when the maximum grows by more than 2^8, and writes P
+//    back over its S row as packed bf16 (the A operand of the PV product).
 //    Columns past the valid keys of a partial page are masked, and the matching
 //    V rows are zeroed before the PV product, so slots past L never matter.
 //  * Work split.  The whole batch is a list of segments (b, g), each a run of
@@ -51,24 +55,26 @@ using namespace sm100;
 
 constexpr int kD = 128;                  // head dim
 constexpr int kPage = 64;                // tokens per page = keys per tile
-constexpr int kStages = 3;               // K/V ring depth
+constexpr int kKStages = 4;              // K ring depth (a stage is free once QK has read it)
+constexpr int kVStages = 6;              // V ring depth (a stage is free once PV has read it)
 constexpr int kMaxCtas = 296;            // upper bound of the persistent grid (sizes the workspace)
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
-// Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kHalf = 8192;              // 64 rows x 128 bytes: one swizzle-128 K-major half tile
+// Shared memory (offsets from a 1024-byte aligned base).  Every tile is stored as two
+// 128-byte-swizzled halves of 64 columns (d 0..63 and d 64..127).
+constexpr int kHalf = 8192;              // 64 rows x 128 bytes
+constexpr int kTile = 2 * kHalf;         // one K or V page
 constexpr int kQTile = 16384;            // 128 rows x 128 bytes
-constexpr int kOffQ = 0;                 // [mt][d-half] 16 KB each
-constexpr int kOffKV = 4 * kQTile;       // [stage] K0 K1 V0 V1
-constexpr int kStageBytes = 4 * kHalf;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;   // [mt] 16 KB each
-constexpr int kSmemBytes = kOffP + 2 * kQTile + 1024;
+constexpr int kOffQ = 0;                 // Q[mt][d-half], 16 KB each
+constexpr int kOffK = 4 * kQTile;
+constexpr int kOffV = kOffK + kKStages * kTile;
+constexpr int kSmemBytes = kOffV + kVStages * kTile + 1024;
 
 // TMEM columns.
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;                 // O[mt]: 128 columns each
-constexpr int kColS = 256;               // S[buf][mt]: 64 columns each
+constexpr int kColS = 256;               // S[buf][mt]: 64 fp32 columns; P overwrites the first 32 as bf16 pairs
 
 struct TcParams {
     const int32_t *page_table;
@@ -87,12 +93,15 @@ struct TcParams {
 
 struct Bars {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, p_empty;
-    uint64_t o_full, o_empty;
-    uint64_t grp;          // softmax warps among themselves (bounded, unlike bar.sync)
-    uint64_t done;
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full[2][2];   // [buffer][M tile]: S of the tile is in TMEM
+    uint64_t s_free[2][2];   // the PV product that read P from this buffer has completed
+    uint64_t p_full[2][2];   // the M tile's four softmax warps wrote P; one per buffer so a warp
+                             // already on tile t+1 cannot complete tile t's phase
+    uint64_t o_full[2], o_empty[2];
+    uint64_t grp;            // softmax warps among themselves (bounded, unlike bar.sync)
+    uint64_t done[3];        // last MMA of each issuer has completed
 };
 
 struct Shared {
@@ -203,42 +212,11 @@ __device__ __forceinline__ int tile_valid(const Piece &pc, int i, int S) {
     return i < pc.ntc ? min(kPage, pc.L - kPage * i) : S;
 }
 
-// PV product of one tile (MMA warp): O[mt] (+)= P[mt] V for every M tile.  `first` /
-// `last`: position of the tile in its piece.  Rows [valid, nk) of a partial page are
-// zeroed in shared memory first, so stale or non-finite slots past L contribute 0.
-__device__ __forceinline__ bool do_pv(Shared &sh, unsigned char *sm, uint32_t tmem, const TcParams &p, int st,
-                                      int valid, int nk, bool first, bool last, int &k_pv, int pi) {
-    Bars &bar = sh.bar;
-    const int lane = threadIdx.x & 31;
-    if (!wait_bar(sh, &bar.p_full, k_pv & 1, p.dev_err)) return false;
-    if (first && !wait_bar(sh, &bar.o_empty, (pi & 1) ^ 1, p.dev_err)) return false;
-    unsigned char *v0 = sm + kOffKV + st * kStageBytes + 2 * kHalf;
-    if (valid < nk) {
-        const int words = (nk - valid) * 8;   // 16-byte words per half
-        for (int w = lane; w < 2 * words; w += 32) {
-            const int h = w / words, r = valid + (w % words) / 8, c = w % 8;
-            *reinterpret_cast<uint4 *>(v0 + h * kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-    }
-    __syncwarp();
-    tc_fence_after();
-    if (lane == 0) {
-        const uint32_t idesc_pv = idesc_bf16_f32(128, kD, false, true);
-        for (int mt = 0; mt < p.NT; ++mt) {
-            const uint32_t pa = smem_u32(sm + kOffP + mt * kQTile);
-            for (int kk = 0; kk < nk / 16; ++kk) {
-                mma_bf16_ss(tmem + kColO + 128 * mt, sdesc_sw128(pa + kk * 32, 16, 1024),
-                            sdesc_sw128(smem_u32(v0) + kk * 2048, kHalf, 1024), idesc_pv, !(first && kk == 0));
-            }
-        }
-        mma_commit(&bar.kv_empty[st]);
-        mma_commit(&bar.p_empty);
-        if (last) mma_commit(&bar.o_full);
-    }
-    __syncwarp();
-    ++k_pv;
-    return true;
+// One elected lane of a converged warp issues each MMA, so the operands stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+    return pred != 0;
 }
 
 // Does CTA c own at least one tile of the segment starting at unit X with ntc page tiles?
@@ -248,9 +226,34 @@ __device__ __forceinline__ bool owns_tile(int c, long long X, int ntc, long long
     return i0 <= ntc && X + 4 * i0 < hi_c;
 }
 
-// ------------------------------------------------------------------ the kernel
+// exp2 of 32 scores of a row -> 16 packed bf16 pairs; columns at or past `valid` give 0.
+template <bool kMasked>
+__device__ __forceinline__ float softmax_half(const uint32_t (&sv)[32], int col0, int valid, float c2, float m,
+                                              uint32_t (&pw)[16]) {
+    float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float a = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c2, -m));
+        float b = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c2, -m));
+        if (kMasked) {
+            a = (col0 + 2 * k < valid) ? a : 0.f;
+            b = (col0 + 2 * k + 1 < valid) ? b : 0.f;
+        }
+        sum0 += a;
+        sum1 += b;
+        pw[k] = pack_bf16(a, b);
+    }
+    return sum0 + sum1;
+}
 
-__global__ void __launch_bounds__(320, 1)
+// ------------------------------------------------------------------ the kernel
+//
+// Warps: 0 TMA producer; 1 and 2 issue QK for M tile 0 and 1; 3 issues PV for every M
+// tile; 4.. softmax, four warps per M tile.  The tensor pipe accepts MMAs from several
+// issuing threads at once, while each issuing thread waits about a hundred cycles per
+// MMA, so QK and PV run on separate issuers.
+
+__global__ void __launch_bounds__(384, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
                const __grid_constant__ CUtensorMap tm_vb, const TcParams p) {
@@ -259,20 +262,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_soft = 4 * p.NT;              // softmax warps
+    const int NT = p.NT;
     Bars &bar = sh.bar;
 
     if (threadIdx.x == 0) {
         mbar_init(&bar.q_full, 1);
-        mbar_init(&bar.q_empty, 1);
-        for (int s = 0; s < kStages; ++s) { mbar_init(&bar.kv_full[s], 1); mbar_init(&bar.kv_empty[s], 1); }
-        for (int s = 0; s < 2; ++s) { mbar_init(&bar.s_full[s], 1); mbar_init(&bar.s_empty[s], n_soft); }
-        mbar_init(&bar.p_full, n_soft);
-        mbar_init(&bar.p_empty, 1);
-        mbar_init(&bar.o_full, 1);
-        mbar_init(&bar.o_empty, n_soft);
-        mbar_init(&bar.grp, n_soft);
-        mbar_init(&bar.done, 1);
+        mbar_init(&bar.q_empty, NT);
+        for (int s = 0; s < kKStages; ++s) { mbar_init(&bar.k_full[s], 1); mbar_init(&bar.k_empty[s], NT); }
+        for (int s = 0; s < kVStages; ++s) { mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1); }
+        for (int s = 0; s < 2; ++s)
+            for (int m = 0; m < 2; ++m) {
+                mbar_init(&bar.s_full[s][m], 1);
+                mbar_init(&bar.s_free[s][m], 1);
+                mbar_init(&bar.p_full[s][m], 4);
+            }
+        for (int m = 0; m < 2; ++m) { mbar_init(&bar.o_full[m], 1); mbar_init(&bar.o_empty[m], 4); }
+        mbar_init(&bar.grp, 4 * NT);
+        for (int i = 0; i < 3; ++i) mbar_init(&bar.done[i], 1);
         fence_mbar_init();
         sh.abort = 0;
         prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
@@ -294,154 +300,224 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (warp == 0) {
         // ================================================================ TMA producer
-        if (lane == 0) {
-            Piece pc;
-            int qi = 0, t = 0;
-            uint32_t stage_parity_pending = 0;   // bit s: a load to stage s was issued
-            uint32_t stage_last_parity = 0;      // parity of that load's phase
-            bool q_pending = false;
-            uint32_t q_last_parity = 0;
-            while (it.next(p, pc)) {
-                if (!wait_bar(sh, &bar.q_empty, (qi & 1) ^ 1, p.dev_err)) break;
-                mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(p.NT * 2 * kQTile));
-                for (int mt = 0; mt < p.NT; ++mt)
+        // The whole warp walks the work (page ids are fetched 32 at a time, one per lane);
+        // lane 0 issues the copies.
+        Piece pc;
+        int qi = 0, t = 0;
+        bool issued = false;
+        while (it.next(p, pc)) {
+            if (!wait_bar(sh, &bar.q_empty, (qi & 1) ^ 1, p.dev_err)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(NT * 2 * kQTile));
+                for (int mt = 0; mt < NT; ++mt)
                     for (int dh = 0; dh < 2; ++dh)
                         tma_load_3d(sm + kOffQ + (2 * mt + dh) * kQTile, &tm_q, &bar.q_full, 64 * dh, pc.g * G,
                                     pc.b * S + mt * (128 / G));
-                q_pending = true;
-                q_last_parity = qi & 1;
-                bool ok = true;
-                for (int i = pc.first; i < pc.last; ++i, ++t) {
-                    const int st = t % kStages;
-                    const uint32_t u = (uint32_t)(t / kStages);
-                    if (!wait_bar(sh, &bar.kv_empty[st], (u & 1) ^ 1, p.dev_err)) { ok = false; break; }
-                    unsigned char *kv = sm + kOffKV + st * kStageBytes;
-                    if (i < pc.ntc) {
-                        int page = p.page_table[(size_t)pc.b * p.max_pages + i];
-                        if (page < 0 || page >= p.num_pages) {
+            }
+            issued = true;
+            bool ok = true;
+            int my_page = 0;
+            for (int i = pc.first; i < pc.last; ++i, ++t) {
+                const int rel = i - pc.first;
+                if ((rel & 31) == 0) {
+                    const int ii = i + lane;
+                    my_page = 0;
+                    if (ii < pc.last && ii < pc.ntc) {
+                        my_page = p.page_table[(size_t)pc.b * p.max_pages + ii];
+                        if (my_page < 0 || my_page >= p.num_pages) {
                             report_error(p.dev_err, TT_ERR_BOUNDS);
-                            page = 0;
+                            my_page = 0;
                         }
-                        mbar_arrive_expect_tx(&bar.kv_full[st], 4 * kHalf);
-                        tma_load_4d(kv, &tm_k, &bar.kv_full[st], 0, 0, pc.g, page);
-                        tma_load_4d(kv + kHalf, &tm_k, &bar.kv_full[st], 64, 0, pc.g, page);
-                        tma_load_4d(kv + 2 * kHalf, &tm_v, &bar.kv_full[st], 0, 0, pc.g, page);
-                        tma_load_4d(kv + 3 * kHalf, &tm_v, &bar.kv_full[st], 64, 0, pc.g, page);
-                    } else {
-                        mbar_arrive_expect_tx(&bar.kv_full[st], (uint32_t)(4 * S * 128));
-                        tma_load_3d(kv, &tm_kb, &bar.kv_full[st], 0, pc.g, pc.b * S);
-                        tma_load_3d(kv + kHalf, &tm_kb, &bar.kv_full[st], 64, pc.g, pc.b * S);
-                        tma_load_3d(kv + 2 * kHalf, &tm_vb, &bar.kv_full[st], 0, pc.g, pc.b * S);
-                        tma_load_3d(kv + 3 * kHalf, &tm_vb, &bar.kv_full[st], 64, pc.g, pc.b * S);
                     }
-                    stage_parity_pending |= 1u << st;
-                    stage_last_parity = (stage_last_parity & ~(1u << st)) | ((u & 1) << st);
+                }
+                const int page = __shfl_sync(0xffffffffu, my_page, rel & 31);
+                const int kst = t % kKStages, vst = t % kVStages;
+                if (!wait_bar(sh, &bar.k_empty[kst], ((uint32_t)(t / kKStages) & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                unsigned char *kd = sm + kOffK + kst * kTile;
+                unsigned char *vd = sm + kOffV + vst * kTile;
+                if (lane == 0) {
+                    if (i < pc.ntc) {
+                        mbar_arrive_expect_tx(&bar.k_full[kst], kTile);
+                        tma_load_4d(kd, &tm_k, &bar.k_full[kst], 0, 0, pc.g, page);
+                        tma_load_4d(kd + kHalf, &tm_k, &bar.k_full[kst], 64, 0, pc.g, page);
+                    } else {
+                        mbar_arrive_expect_tx(&bar.k_full[kst], (uint32_t)(2 * S * 128));
+                        tma_load_3d(kd, &tm_kb, &bar.k_full[kst], 0, pc.g, pc.b * S);
+                        tma_load_3d(kd + kHalf, &tm_kb, &bar.k_full[kst], 64, pc.g, pc.b * S);
+                    }
+                }
+                if (!wait_bar(sh, &bar.v_empty[vst], ((uint32_t)(t / kVStages) & 1) ^ 1, p.dev_err)) {
+                    ok = false;
+                    ++t;   // the K copy of this tile is in flight: count it for the drain
+                    break;
+                }
+                if (lane == 0) {
+                    if (i < pc.ntc) {
+                        mbar_arrive_expect_tx(&bar.v_full[vst], kTile);
+                        tma_load_4d(vd, &tm_v, &bar.v_full[vst], 0, 0, pc.g, page);
+                        tma_load_4d(vd + kHalf, &tm_v, &bar.v_full[vst], 64, 0, pc.g, page);
+                    } else {
+                        mbar_arrive_expect_tx(&bar.v_full[vst], (uint32_t)(2 * S * 128));
+                        tma_load_3d(vd, &tm_vb, &bar.v_full[vst], 0, pc.g, pc.b * S);
+                        tma_load_3d(vd + kHalf, &tm_vb, &bar.v_full[vst], 64, pc.g, pc.b * S);
+                    }
+                }
+            }
+            ++qi;
+            if (!ok) break;
+        }
+        // Drain: every copy issued must land before the CTA may exit.  The last copy into
+        // a stage completes that stage's latest phase.
+        if (issued) mbar_wait(&bar.q_full, (uint32_t)(qi - 1) & 1, kWaitLimit);
+        for (int k = 1; k <= kKStages && t - k >= 0; ++k)
+            mbar_wait(&bar.k_full[(t - k) % kKStages], (uint32_t)((t - k) / kKStages) & 1, kWaitLimit);
+        for (int k = 1; k <= kVStages && t - k >= 0; ++k)
+            mbar_wait(&bar.v_full[(t - k) % kVStages], (uint32_t)((t - k) / kVStages) & 1, kWaitLimit);
+        __syncwarp();
+    } else if (warp == 1 || warp == 2) {
+        // ================================================================ QK issuer of M tile mt
+        const int mt = warp - 1;
+        if (mt < NT) {
+            Piece pc;
+            int qi = 0, t = 0;
+            bool ok = true;
+            const uint32_t qa = smem_u32(sm + kOffQ + 2 * mt * kQTile);
+            while (ok && it.next(p, pc)) {
+                if (!wait_bar(sh, &bar.q_full, qi & 1, p.dev_err)) break;
+                tc_fence_after();
+                const int ntiles = pc.last - pc.first;
+                for (int j = 0; j < ntiles; ++j, ++t) {
+                    const int i = pc.first + j;
+                    const int kst = t % kKStages, sb = t & 1;
+                    const int valid = tile_valid(pc, i, S);
+                    const int nk = (valid + 15) & ~15;
+                    if (!wait_bar(sh, &bar.k_full[kst], (uint32_t)(t / kKStages) & 1, p.dev_err)) { ok = false; break; }
+                    if (!wait_bar(sh, &bar.s_free[sb][mt], (((uint32_t)t >> 1) & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t idesc = idesc_bf16_f32(128, nk, false, false);
+                    const uint32_t kb = smem_u32(sm + kOffK + kst * kTile);
+                    const uint32_t dcol = tmem + kColS + 64 * (2 * sb + mt);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t da = sdesc_sw128(qa + (kk >> 2) * (uint32_t)kQTile + (kk & 3) * 32, 16, 1024);
+                        const uint64_t db = sdesc_sw128(kb + (kk >> 2) * (uint32_t)kHalf + (kk & 3) * 32, 16, 1024);
+                        if (elect_one()) mma_bf16_ss(dcol, da, db, idesc, kk > 0);
+                        __syncwarp();
+                    }
+                    if (elect_one()) {
+                        mma_commit(&bar.s_full[sb][mt]);
+                        mma_commit(&bar.k_empty[kst]);
+                        if (j == ntiles - 1) mma_commit(&bar.q_empty);
+                    }
+                    __syncwarp();
                 }
                 ++qi;
-                if (!ok) break;
             }
-            // Drain: every issued copy must land before the CTA may exit.
-            if (q_pending) mbar_wait(&bar.q_full, q_last_parity, kWaitLimit);
-            for (int st = 0; st < kStages; ++st)
-                if (stage_parity_pending & (1u << st))
-                    mbar_wait(&bar.kv_full[st], (stage_last_parity >> st) & 1, kWaitLimit);
+            if (elect_one()) mma_commit(&bar.done[mt]);
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
+    } else if (warp == 3) {
+        // ================================================================ PV issuer
         Piece pc;
-        int qi = 0, t = 0, k_pv = 0, pi = 0;
+        int t = 0, pi = 0;
         bool ok = true;
+        const uint32_t idesc_pv = idesc_bf16_f32(128, kD, false, true);
         while (ok && it.next(p, pc)) {
-            if (!wait_bar(sh, &bar.q_full, qi & 1, p.dev_err)) break;
-            tc_fence_after();
             const int ntiles = pc.last - pc.first;
-            int prev_st = 0, prev_valid = 0, prev_nk = 0;
-            for (int j = 0; j < ntiles; ++j, ++t) {
+            for (int j = 0; j < ntiles && ok; ++j, ++t) {
                 const int i = pc.first + j;
-                const int st = t % kStages, sb = t & 1;
+                const int vst = t % kVStages, sb = t & 1;
                 const int valid = tile_valid(pc, i, S);
                 const int nk = (valid + 15) & ~15;
-                if (!wait_bar(sh, &bar.kv_full[st], (uint32_t)(t / kStages) & 1, p.dev_err)) { ok = false; break; }
-                if (!wait_bar(sh, &bar.s_empty[sb], (((uint32_t)t >> 1) & 1) ^ 1, p.dev_err)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t idesc = idesc_bf16_f32(128, nk, false, false);
-                    const uint32_t kb = smem_u32(sm + kOffKV + st * kStageBytes);
-                    for (int mt = 0; mt < p.NT; ++mt) {
-                        const uint32_t qa = smem_u32(sm + kOffQ + 2 * mt * kQTile);
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (kk >> 2) * (uint32_t)kQTile + (kk & 3) * 32;
-                            const uint32_t koff = (kk >> 2) * (uint32_t)kHalf + (kk & 3) * 32;
-                            mma_bf16_ss(tmem + kColS + 64 * (2 * sb + mt), sdesc_sw128(qa + off, 16, 1024),
-                                        sdesc_sw128(kb + koff, 16, 1024), idesc, kk > 0);
-                        }
+                if (!wait_bar(sh, &bar.v_full[vst], (uint32_t)(t / kVStages) & 1, p.dev_err)) { ok = false; break; }
+                unsigned char *v0 = sm + kOffV + vst * kTile;
+                if (valid < nk) {
+                    // rows [valid, nk) of this page are past the context: zero them in both halves
+                    const int words = (nk - valid) * 8;   // 16-byte words per half
+                    for (int w = lane; w < 2 * words; w += 32) {
+                        const int h = w / words, r = valid + (w % words) / 8, c = w % 8;
+                        *reinterpret_cast<uint4 *>(v0 + h * kHalf + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
                     }
-                    mma_commit(&bar.s_full[sb]);
-                    if (j == ntiles - 1) mma_commit(&bar.q_empty);
+                    fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (j > 0 && !do_pv(sh, sm, tmem, p, prev_st, prev_valid, prev_nk, j == 1, false, k_pv, pi)) { ok = false; break; }
-                prev_st = st; prev_valid = valid; prev_nk = nk;
+                for (int mt = 0; mt < NT; ++mt) {
+                    if (!wait_bar(sh, &bar.p_full[sb][mt], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
+                    if (j == 0 && !wait_bar(sh, &bar.o_empty[mt], (pi & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t pcol = tmem + kColS + 64 * (2 * sb + mt);
+                    for (int kk = 0; kk < nk / 16; ++kk) {
+                        const uint64_t dv = sdesc_sw128(smem_u32(v0) + kk * 2048, kHalf, 1024);
+                        if (elect_one()) mma_bf16_ts(tmem + kColO + 128 * mt, pcol + 8 * kk, dv, idesc_pv, !(j == 0 && kk == 0));
+                        __syncwarp();
+                    }
+                    if (elect_one()) {
+                        mma_commit(&bar.s_free[sb][mt]);
+                        if (j == ntiles - 1) mma_commit(&bar.o_full[mt]);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (elect_one()) mma_commit(&bar.v_empty[vst]);
+                __syncwarp();
             }
-            if (!ok) break;
-            if (!do_pv(sh, sm, tmem, p, prev_st, prev_valid, prev_nk, ntiles == 1, true, k_pv, pi)) { ok = false; break; }
-            ++qi;
             ++pi;
         }
-        // Completion of everything issued so far, before TMEM may be released.
-        if (lane == 0) mma_commit(&bar.done);
+        if (elect_one()) mma_commit(&bar.done[2]);
         __syncwarp();
-    } else if (warp >= 2 && warp < 2 + n_soft) {
+    } else if (warp >= 4 && warp < 4 + 4 * NT) {
         // ================================================================ softmax / epilogue
-        const int mt = (warp - 2) >> 2, wq = warp & 3;   // each run of 4 warps covers all TMEM lane quarters
-        const int r_local = 32 * wq + lane;
-        const int r = 128 * mt + r_local;          // row of the segment: r = s * G + hh
+        const int mt = (warp - 4) >> 2, wq = warp & 3;
+        const int r = 128 * mt + 32 * wq + lane;         // row of the segment: r = s * G + hh
         const int s_pos = r / G, hh = r % G;
         const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
-        unsigned char *prow = sm + kOffP + mt * kQTile + r_local * 128;
         const float c2 = p.scale_log2;
         Piece pc;
-        int t = 0, k_p = 0, pi = 0, k_grp = 0;
+        int t = 0, pi = 0, k_grp = 0;
         bool ok = true;
         while (ok && it.next(p, pc)) {
             float m_used = -INFINITY, l = 0.f;
             const int ntiles = pc.last - pc.first;
             for (int j = 0; j < ntiles; ++j, ++t) {
                 const int i = pc.first + j;
-                const int sb_i = t & 1;
+                const int sb = t & 1;
                 const int valid = tile_valid(pc, i, S);
-                const int nk = (valid + 15) & ~15;
-                if (!wait_bar(sh, &bar.s_full[sb_i], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
+                if (!wait_bar(sh, &bar.s_full[sb][mt], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t sa[32], sb[32];
-                const uint32_t scol = tmem + lane_off + kColS + 64 * (2 * sb_i + mt);
+                const uint32_t scol = tmem + lane_off + kColS + 64 * (2 * sb + mt);
+                uint32_t sa[32], sc[32];
                 tmem_ld32(scol, sa);
-                if (nk > 32) tmem_ld32(scol + 32, sb);
+                if (valid > 32) tmem_ld32(scol + 32, sc);
                 tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.s_empty[sb_i]);
-                float mx = -INFINITY;
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+                if (valid == kPage) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    if (k < valid) mx = fmaxf(mx, __uint_as_float(sa[k]));
-                    if (k + 32 < valid) mx = fmaxf(mx, __uint_as_float(sb[k]));
+                    for (int k = 0; k < 32; ++k) {
+                        mx0 = fmaxf(mx0, __uint_as_float(sa[k]));
+                        mx1 = fmaxf(mx1, __uint_as_float(sc[k]));
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        if (k < valid) mx0 = fmaxf(mx0, __uint_as_float(sa[k]));
+                        if (k + 32 < valid) mx1 = fmaxf(mx1, __uint_as_float(sc[k]));
+                    }
                 }
-                const float mt2 = mx * c2;
+                const float mt2 = fmaxf(mx0, mx1) * c2;
                 const bool resc = mt2 > m_used + kRescaleThreshold;
                 float alpha = 1.f;
                 if (resc) {
                     alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - mt2);
                     m_used = mt2;
                 }
-                // O rescale first (rare: the row maximum grew by more than 2^8), warp-uniform since
-                // tcgen05.ld/st are warp-collective; lanes whose maximum did not move scale by 1.
-                bool p_free = false;
+                // O rescale (rare: the row maximum grew by more than 2^8) once PV(t-1) is done;
+                // warp-uniform because tcgen05.ld/st are warp-collective.
                 if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                    if (!wait_bar(sh, &bar.p_empty, (k_p & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                    if (!wait_bar(sh, &bar.s_free[(t - 1) & 1][mt], ((uint32_t)(t - 1) >> 1) & 1, p.dev_err)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    p_free = true;
                     for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
                         const uint32_t ocol = tmem + lane_off + kColO + 128 * mt + 32 * ch;
@@ -450,46 +526,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                         for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
                         tmem_st32(ocol, o);
+                        tmem_wait_st();   // o is reused by the next chunk
                     }
-                    tmem_wait_st();
                 }
-                float psum = 0.f;
-                uint32_t pw[32];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float a0 = (2 * k < valid) ? fast_exp2(fmaf(__uint_as_float(sa[2 * k]), c2, -m_used)) : 0.f;
-                    const float a1 = (2 * k + 1 < valid) ? fast_exp2(fmaf(__uint_as_float(sa[2 * k + 1]), c2, -m_used))
-                                                         : 0.f;
-                    const float b0 = (2 * k + 32 < valid) ? fast_exp2(fmaf(__uint_as_float(sb[2 * k]), c2, -m_used))
-                                                          : 0.f;
-                    const float b1 = (2 * k + 33 < valid)
-                                         ? fast_exp2(fmaf(__uint_as_float(sb[2 * k + 1]), c2, -m_used))
-                                         : 0.f;
-                    psum += (a0 + a1) + (b0 + b1);
-                    pw[k] = pack_bf16(a0, a1);
-                    pw[16 + k] = pack_bf16(b0, b1);
+                // tcgen05.st reads its source registers asynchronously: each half has its own
+                // registers, and nothing reuses them before tcgen05.wait::st.
+                uint32_t pw0[16], pw1[16];
+                float psum;
+                if (valid == kPage) {
+                    psum = softmax_half<false>(sa, 0, valid, c2, m_used, pw0);
+                    psum += softmax_half<false>(sc, 32, valid, c2, m_used, pw1);
+                    tmem_st16(scol, pw0);
+                    tmem_st16(scol + 16, pw1);
+                } else {
+                    psum = softmax_half<true>(sa, 0, valid, c2, m_used, pw0);
+                    tmem_st16(scol, pw0);
+                    if (valid > 32) {
+                        psum += softmax_half<true>(sc, 32, valid, c2, m_used, pw1);
+                        tmem_st16(scol + 16, pw1);
+                    }
                 }
+                tmem_wait_st();
                 l = l * alpha + psum;
-                if (!p_free) {
-                    if (!wait_bar(sh, &bar.p_empty, (k_p & 1) ^ 1, p.dev_err)) { ok = false; break; }
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    if (8 * c < nk) {
-                        *reinterpret_cast<uint4 *>(prow + ((c ^ (r_local & 7)) << 4)) =
-                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.p_full);
-                ++k_p;
+                if (lane == 0) mbar_arrive(&bar.p_full[sb][mt]);
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue of the piece
-            if (!wait_bar(sh, &bar.o_full, pi & 1, p.dev_err)) { ok = false; break; }
+            if (!wait_bar(sh, &bar.o_full[mt], pi & 1, p.dev_err)) { ok = false; break; }
             tc_fence_after();
             const int hq = pc.g * G + hh;
             if (pc.whole) {
@@ -512,11 +577,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (p.lse) p.lse[((size_t)pc.b * p.Hq + hq) * S + s_pos] = (m_used + __log2f(l)) * kLn2;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.o_empty);
+                if (lane == 0) mbar_arrive(&bar.o_empty[mt]);
             } else {
                 // partial: unnormalised O, the row maximum used (log2 units) and the row sum
-                const int cta = blockIdx.x;
-                float *slot = p.part + (long long)(cta + pc.sg) * p.slot_floats;
+                float *slot = p.part + (long long)(blockIdx.x + pc.sg) * p.slot_floats;
                 float *orow = slot + (size_t)r * kD;
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t o[32];
@@ -532,10 +596,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 __stcg(slot + (size_t)p.rows * kD + p.rows + r, l);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.o_empty);
+                if (lane == 0) mbar_arrive(&bar.o_empty[mt]);
                 __threadfence();
                 if (!group_sync(sh, k_grp, p.dev_err)) { ok = false; break; }
-                if (threadIdx.x == 64) {
+                if (threadIdx.x == 128) {
                     const unsigned n_here = (unsigned)(pc.last - pc.first);
                     const unsigned before = atomicAdd(&p.tickets[pc.sg], n_here);
                     sh.last = (before + n_here == (unsigned)(pc.ntc + 1));
@@ -590,7 +654,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         }
                     }
                     if (p.lse) p.lse[((size_t)pc.b * p.Hq + hq) * S + s_pos] = (M + __log2f(Lsum)) * kLn2;
-                    if (threadIdx.x == 64) p.tickets[pc.sg] = 0;   // ready for the next launch
+                    if (threadIdx.x == 128) p.tickets[pc.sg] = 0;   // ready for the next launch
                 }
             }
             ++pi;
@@ -602,7 +666,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        mbar_wait(&bar.done, 0, kWaitLimit);      // every MMA of this CTA has completed
+        // every MMA of this CTA has completed (each issuer committed its last one)
+        for (int i = 0; i < NT; ++i) mbar_wait(&bar.done[i], 0, kWaitLimit);
+        mbar_wait(&bar.done[2], 0, kWaitLimit);
         tmem_dealloc(tmem, kTmemCols);
     }
 }
@@ -705,7 +771,7 @@ tt_status launch_attn_tc(const AttnArgs &a) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return TT_ERR_CUDA;
-    attn_tc_kernel<<<n, 64 + 128 * NT, kSmemBytes, a.stream>>>(mq, mk, mv, mkb, mvb, p);
+    attn_tc_kernel<<<n, 128 + 128 * NT, kSmemBytes, a.stream>>>(mq, mk, mv, mkb, mvb, p);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
