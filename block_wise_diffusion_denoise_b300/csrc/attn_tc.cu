@@ -23,11 +23,15 @@
 //    double-buffered TMEM tile, another issues O += P V (M 128, N 128 = D,
 //    K 128 keys) with P read from TMEM; one elected lane of a converged warp
 //    issues, so the descriptors stay warp-uniform.
-//  * Softmax.  Two threads per row (two warps share each TMEM lane quarter)
-//    each read 64 of the row's 128 scores from TMEM, exchange their maxima
-//    through shared memory, keep the running maximum in the log2 domain and only
-//    rescale O (in TMEM) when it grows by more than 2^8, and write P as packed
-//    bf16 into its own double-buffered TMEM tile.  Columns past the valid keys of a partial tile
+//  * Softmax.  Two warps share each TMEM lane quarter and take alternate tiles,
+//    one thread per row: the row's 128 scores come into registers at once and
+//    the S buffer goes back to the QK issuer immediately; the running maximum
+//    (log2 domain) is taken over from the partner's previous tile and only
+//    raised -- with a rescale of O in TMEM -- when the tile exceeds it by more
+//    than 2^8; P is written as packed bf16 into its own double-buffered TMEM
+//    tile.  The exponent phase of one tile overlaps the next QK product and the
+//    score phase of the partner's tile.  A register split (setmaxnreg) gives the
+//    softmax warpgroups 216 registers per thread and the role warps 64.  Columns past the valid keys of a partial tile
 //    are masked, and the matching V rows are zeroed before the PV product, so
 //    slots past L never matter.
 //  * Work split.  The batch is a list of segments (b, g), each a run of
@@ -102,10 +106,10 @@ struct Bars {
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2];    // S of the tile is in TMEM (QK committed)
-    uint64_t s_empty[2];   // the softmax warps have read S (eight arrivals)
-    uint64_t p_full[2];    // the softmax warps wrote P (eight arrivals)
+    uint64_t s_empty[2];   // the tile's four softmax warps have read S
+    uint64_t p_full[2];    // the tile's four softmax warps wrote P
     uint64_t p_free[2];    // the PV product that read P has completed
-    uint64_t pair[2][4];   // the two softmax warps of a lane quarter exchanged their row maxima
+    uint64_t pub[2][4];    // [tile parity][lane quarter]: the running maximum after the tile is published
     uint64_t o_full, o_empty;
     uint64_t grp;          // softmax warps among themselves (bounded, unlike bar.sync)
     uint64_t done[2];      // last MMA of each issuer has completed
@@ -113,8 +117,9 @@ struct Bars {
 
 struct Shared {
     Bars bar;
-    float red[2][2][128];  // [buffer][half][row]: half-row maxima of the current tile
-    float lsum[2][128];    // [half][row]: half-row sums at the end of a piece
+    float mpub[2][128];    // [tile parity][row]: running maximum after the tile (log2 units)
+    float lsum[2][128];    // [warp half][row]: row sums at the end of a piece
+    float lmax[2][128];    // [warp half][row]: the maximum each row sum is scaled by
     uint32_t tmem_base;
     int abort;
     int last;
@@ -225,6 +230,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+// Register split between warpgroups: the launch gives 384 x 168 registers; the role
+// warpgroup (warps 0-3) drops to 64 each and the two softmax warpgroups rise to 216
+// each (128 x 64 + 256 x 216 = 63488 <= 64512).
+__device__ __forceinline__ void regs_release() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;"); }
+__device__ __forceinline__ void regs_acquire() { asm volatile("setmaxnreg.inc.sync.aligned.u32 216;"); }
+
 // One elected lane of a converged warp issues each MMA, so the operands stay warp-uniform.
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred;
@@ -275,7 +286,8 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&sv)[32], int col0, i
 // ------------------------------------------------------------------ the kernel
 //
 // Warps: 0 TMA producer; 1 QK issuer; 2 PV issuer; 3 idle; 4..11 softmax and epilogue
-// (two threads per row of the CTA's M tile, each with half of the keys and of O).
+// (two warps per TMEM lane quarter taking alternate tiles; at the end of a piece each
+// writes half of the O columns).
 
 __global__ void __launch_bounds__(384, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -296,10 +308,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int s = 0; s < kVStages; ++s) { mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1); }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar.s_full[s], 1);
-            mbar_init(&bar.s_empty[s], 8);
-            mbar_init(&bar.p_full[s], 8);
+            mbar_init(&bar.s_empty[s], 4);
+            mbar_init(&bar.p_full[s], 4);
             mbar_init(&bar.p_free[s], 1);
-            for (int q = 0; q < 4; ++q) mbar_init(&bar.pair[s][q], 2);
+            for (int q = 0; q < 4; ++q) mbar_init(&bar.pub[s][q], 1);
         }
         mbar_init(&bar.o_full, 1);
         mbar_init(&bar.o_empty, 8);
@@ -325,6 +337,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int S = p.S, G = p.G;
 
     if (warp == 0) {
+        regs_release();
         // ================================================================ TMA producer
         // The whole warp walks the work (page ids are fetched 32 at a time, one per lane);
         // lane 0 issues the copies.
@@ -413,6 +426,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_wait(&bar.v_full[(t - k) % kVStages], (uint32_t)((t - k) / kVStages) & 1, kWaitLimit);
         __syncwarp();
     } else if (warp == 1) {
+        regs_release();
         // ================================================================ QK issuer
         Piece pc;
         int qi = 0, t = 0;
@@ -451,6 +465,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (elect_one()) mma_commit(&bar.done[0]);
         __syncwarp();
     } else if (warp == 2) {
+        regs_release();
         // ================================================================ PV issuer
         Piece pc;
         int t = 0, pi = 0;
@@ -504,10 +519,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (elect_one()) mma_commit(&bar.done[1]);
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp == 3) {
+        regs_release();   // idle warp of the role warpgroup
+    } else {
+        regs_acquire();
         // ================================================================ softmax / epilogue
-        // Two threads per row: warp 4 + q and warp 8 + q both read TMEM lanes 32q..32q+31;
-        // half h takes keys [64h, 64h + 64) of every tile and O columns [64h, 64h + 64).
+        // Warps 4 + q and 8 + q both read TMEM lanes 32q..32q+31 (rows of quarter q) and
+        // take alternate tiles (half h = t & 1), so the exponent phase of tile t overlaps
+        // the score phase of tile t+1.  Only the running maximum passes from one to the
+        // next (one-directional, through shared memory); each keeps its own row sum in
+        // the scale of the last maximum it used.
         const int wq = warp & 3, h = (warp - 4) >> 2;
         const int rl = 32 * wq + lane;                   // row within the M tile
         const int r = 128 * mt + rl;                     // row of the segment: r = s * G + hh
@@ -518,58 +539,67 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int t = 0, pi = 0, k_grp = 0;
         bool ok = true;
         while (ok && it.next(p, pc)) {
-            float m_used = -INFINITY, l = 0.f;
+            float m_l = -INFINITY, l = 0.f;              // my row sum and the maximum it is scaled by
+            float m_last = -INFINITY;                    // maximum after my latest tile
             const int ntiles = pc.last - pc.first;
             for (int j = 0; j < ntiles; ++j, ++t) {
-                const int sb = t & 1;
+                if ((t & 1) != h) continue;              // the partner's tile
+                const int sb = h;
                 const int valid = tile_valid(pc, pc.first + j, S);
-                const int vh = min(max(valid - 64 * h, 0), 64);   // valid keys of this half
                 if (!wait_bar(sh, &bar.s_full[sb], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t scol = tmem + lane_off + kColS + 128 * sb + 64 * h;
-                uint32_t s0[32], s1[32];
-                if (vh > 0) tmem_ld32(scol, s0);
-                if (vh > 32) tmem_ld32(scol + 32, s1);
+                const uint32_t scol = tmem + lane_off + kColS + 128 * sb;
+                // ---- the row's 128 scores into registers (all loads in flight at once), its
+                // maximum, and S released to the next QK product right away
+                uint32_t a0[32], a1[32], a2[32], a3[32];
+                tmem_ld32(scol, a0);
+                if (valid > 32) tmem_ld32(scol + 32, a1);
+                if (valid > 64) tmem_ld32(scol + 64, a2);
+                if (valid > 96) tmem_ld32(scol + 96, a3);
                 tmem_wait_ld();
-                float mx = -INFINITY;
-                if (vh == 64) {
-                    mx = fmaxf(chunk_max<false>(s0, 0, vh), chunk_max<false>(s1, 32, vh));
-                } else {
-                    if (vh > 0) mx = chunk_max<true>(s0, 0, vh);
-                    if (vh > 32) mx = fmaxf(mx, chunk_max<true>(s1, 32, vh));
-                }
-                // exchange the half maxima of the row with the partner thread
-                sh.red[sb][h][rl] = mx;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.pair[sb][wq]);
-                if (!wait_bar(sh, &bar.pair[sb][wq], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
-                mx = fmaxf(mx, sh.red[sb][h ^ 1][rl]);
-                // S is in registers and the partner has read our maximum: the buffer may take
-                // the next QK product
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
-                const float mt2 = mx * c2;
-                const bool resc = mt2 > m_used + kRescaleThreshold;
-                float alpha = 1.f;
-                if (resc) {
-                    alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - mt2);
-                    m_used = mt2;
+                float mx;
+                if (valid == kTileKeys) {
+                    mx = fmaxf(fmaxf(chunk_max<false>(a0, 0, valid), chunk_max<false>(a1, 32, valid)),
+                               fmaxf(chunk_max<false>(a2, 64, valid), chunk_max<false>(a3, 96, valid)));
+                } else {
+                    mx = chunk_max<true>(a0, 0, valid);
+                    if (valid > 32) mx = fmaxf(mx, chunk_max<true>(a1, 32, valid));
+                    if (valid > 64) mx = fmaxf(mx, chunk_max<true>(a2, 64, valid));
+                    if (valid > 96) mx = fmaxf(mx, chunk_max<true>(a3, 96, valid));
                 }
+                // ---- the running maximum: the previous tile's (from the partner), raised when
+                // this tile's maximum exceeds it by more than 2^8
+                float m_prev = -INFINITY;
+                if (j > 0) {
+                    if (!wait_bar(sh, &bar.pub[(t - 1) & 1][wq], ((uint32_t)(t - 1) >> 1) & 1, p.dev_err)) {
+                        ok = false;
+                        break;
+                    }
+                    m_prev = sh.mpub[(t - 1) & 1][rl];
+                }
+                const float mt2 = mx * c2;
+                const float m_t = (mt2 > m_prev + kRescaleThreshold) ? mt2 : m_prev;
+                sh.mpub[t & 1][rl] = m_t;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar.pub[t & 1][wq]);
                 // P buffer sb is free once the PV product of tile t-2 has completed.
                 if (!wait_bar(sh, &bar.p_free[sb], (((uint32_t)t >> 1) & 1) ^ 1, p.dev_err)) { ok = false; break; }
-                // O rescale (rare: the row maximum grew by more than 2^8) also needs PV(t-1)
-                // done; warp-uniform because tcgen05.ld/st are warp-collective.  Each half
-                // scales its own 64 columns of O.
-                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                // O rescale (rare: the maximum moved at this tile) between PV(t-1) and PV(t);
+                // warp-uniform because tcgen05.ld/st are warp-collective.
+                const bool moved = j > 0 && m_t != m_prev;
+                if (__any_sync(0xffffffffu, moved)) {
                     if (!wait_bar(sh, &bar.p_free[sb ^ 1], ((uint32_t)(t - 1) >> 1) & 1, p.dev_err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int ch = 0; ch < 2; ++ch) {
+                    const float alpha = moved ? fast_exp2(m_prev - m_t) : 1.f;
+                    for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
-                        const uint32_t ocol = tmem + lane_off + kColO + 64 * h + 32 * ch;
+                        const uint32_t ocol = tmem + lane_off + kColO + 32 * ch;
                         tmem_ld32(ocol, o);
                         tmem_wait_ld();
 #pragma unroll
@@ -579,28 +609,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
                 tc_fence_after();
-                // tcgen05.st reads its source registers asynchronously: every chunk has its own
-                // registers, and nothing reuses them before tcgen05.wait::st.
-                const uint32_t pcolt = tmem + lane_off + kColP + 64 * sb + 32 * h;
-                uint32_t p0[16], p1[16];
-                float psum = 0.f;
-                if (vh == 64) {
-                    psum = softmax_chunk<false>(s0, 0, vh, c2, m_used, p0);
-                    tmem_st16(pcolt, p0);
-                    psum += softmax_chunk<false>(s1, 32, vh, c2, m_used, p1);
-                    tmem_st16(pcolt + 16, p1);
+                if (m_l != -INFINITY && m_l != m_t) l *= fast_exp2(m_l - m_t);
+                m_l = m_t;
+                m_last = m_t;
+                // ---- P = 2^(s*c - m_t) as packed bf16 into TMEM (tcgen05.st takes its source
+                // registers at issue; tcgen05.wait::st below orders the TMEM writes before the PV
+                // product)
+                const uint32_t pcolt = tmem + lane_off + kColP + 64 * sb;
+                float psum;
+                uint32_t pw[16];
+                if (valid == kTileKeys) {
+                    psum = softmax_chunk<false>(a0, 0, valid, c2, m_t, pw);
+                    tmem_st16(pcolt, pw);
+                    psum += softmax_chunk<false>(a1, 32, valid, c2, m_t, pw);
+                    tmem_st16(pcolt + 16, pw);
+                    psum += softmax_chunk<false>(a2, 64, valid, c2, m_t, pw);
+                    tmem_st16(pcolt + 32, pw);
+                    psum += softmax_chunk<false>(a3, 96, valid, c2, m_t, pw);
+                    tmem_st16(pcolt + 48, pw);
                 } else {
-                    if (vh > 0) {
-                        psum = softmax_chunk<true>(s0, 0, vh, c2, m_used, p0);
-                        tmem_st16(pcolt, p0);
+                    psum = softmax_chunk<true>(a0, 0, valid, c2, m_t, pw);
+                    tmem_st16(pcolt, pw);
+                    if (valid > 32) {
+                        psum += softmax_chunk<true>(a1, 32, valid, c2, m_t, pw);
+                        tmem_st16(pcolt + 16, pw);
                     }
-                    if (vh > 32) {
-                        psum += softmax_chunk<true>(s1, 32, vh, c2, m_used, p1);
-                        tmem_st16(pcolt + 16, p1);
+                    if (valid > 64) {
+                        psum += softmax_chunk<true>(a2, 64, valid, c2, m_t, pw);
+                        tmem_st16(pcolt + 32, pw);
+                    }
+                    if (valid > 96) {
+                        psum += softmax_chunk<true>(a3, 96, valid, c2, m_t, pw);
+                        tmem_st16(pcolt + 48, pw);
                     }
                 }
                 tmem_wait_st();
-                l = l * alpha + psum;
+                l += psum;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.p_full[sb]);
@@ -609,10 +653,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // ---------------------------------------------------------- epilogue of the piece
             if (!wait_bar(sh, &bar.o_full, pi & 1, p.dev_err)) { ok = false; break; }
             tc_fence_after();
-            // the row sum is split between the two halves
+            // merge the two row sums in the scale of the final maximum (the larger of the two)
             sh.lsum[h][rl] = l;
+            sh.lmax[h][rl] = m_last;
             if (!group_sync(sh, k_grp, p.dev_err)) { ok = false; break; }
-            l += sh.lsum[h ^ 1][rl];
+            {
+                const float l2 = sh.lsum[h ^ 1][rl], m2 = sh.lmax[h ^ 1][rl];
+                const float mf = fmaxf(m_last, m2);
+                l = (m_last == -INFINITY ? 0.f : l * fast_exp2(m_last - mf)) +
+                    (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - mf));
+                m_last = mf;
+            }
+            const float m_used = m_last;
             const int hq = pc.g * G + hh;
             if (pc.whole) {
                 const float inv = 1.f / l;
