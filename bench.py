@@ -326,8 +326,9 @@ def run_ours(a, cfg):
         api.tt_denoise_attn(c["cache"], c["q"], c["kb"], c["vb"], out=c["out"], sm_scale=scale, ws=attn_ws,
                             dev_err=err, stream=stream)
 
-    unm_masked = torch.ones((n_state, cfg.B, cfg.S), dtype=torch.uint8, device=dev)
-    unm_tokens = torch.full((n_state, cfg.B, cfg.S), -1, dtype=torch.int32, device=dev)
+    k_ker = max(10, min(a.steps, 200))   # launches per kernel-only timing
+    unm_masked = torch.ones((k_ker, cfg.B, cfg.S), dtype=torch.uint8, device=dev)
+    unm_tokens = torch.full((k_ker, cfg.B, cfg.S), -1, dtype=torch.int32, device=dev)
 
     def unmask_only(i, stream=None):
         c = copies[i % n_copies]
@@ -411,7 +412,6 @@ def run_ours(a, cfg):
         raise SystemExit("a timed step committed nothing")
 
     # ---- per-kernel durations (CUDA events on the launching stream), same rotation of inputs
-    k_ker = max(10, min(a.steps, 200))
     attn_ms = timed(attn_only, 0, k_ker, use_graph) / k_ker
     unm_masked.fill_(1)
     unmask_ms = timed(unmask_only, 0, k_ker, use_graph) / k_ker

@@ -16,9 +16,10 @@
 //    page is served by L2 and HBM sees each byte once.  One M tile per CTA
 //    leaves room in tensor memory for double-buffered 128-key S and P tiles.
 //  * Tiles.  A key tile is two 64-token pages of the paged cache (or the block's
-//    own S keys).  A producer warp moves them with TMA (128-byte swizzle) into
+//    own S keys).  Two producer warps move them with TMA (128-byte swizzle) into
 //    separate K and V rings (a K stage is free once QK has read it, a V stage
-//    once PV has), fetching page ids 32 at a time; Q is loaded once per piece.
+//    once PV has), each fetching page ids 32 at a time; Q is loaded once per
+//    piece.
 //  * MMAs.  One warp issues S = Q K^T (M 128, N 128 keys) into a
 //    double-buffered TMEM tile, another issues O += P V (M 128, N 128 = D,
 //    K 128 keys) with P read from TMEM; one elected lane of a converged warp
@@ -77,7 +78,13 @@ constexpr int kStage = 2 * kHalf;        // one K or V tile (128 keys x 128 d)
 constexpr int kOffQ = 0;                 // Q[d-half]
 constexpr int kOffK = kStage;
 constexpr int kOffV = kOffK + kKStages * kStage;
-constexpr int kSmemBytes = kOffV + kVStages * kStage + 1024;
+// Per-sequence table of one launch: clamped context lengths and the prefix sums of the
+// sequences' work units (at most kSeqMax sequences per launch; the host splits larger
+// batches into several launches).
+constexpr int kSeqMax = 1024;
+constexpr int kOffSeqPre = kOffV + kVStages * kStage;               // long long [kSeqMax + 1]
+constexpr int kOffSeqLen = kOffSeqPre + 8 * (kSeqMax + 1);          // int [kSeqMax]
+constexpr int kSmemBytes = kOffSeqLen + 4 * kSeqMax + 1024;
 
 // TMEM columns (one M tile per CTA).
 constexpr int kTmemCols = 512;
@@ -127,9 +134,8 @@ struct Shared {
 
 // ------------------------------------------------------------------ work partition
 
-__device__ __forceinline__ int clamp_len(const TcParams &p, int b) {
-    const int L = p.ctx_len[b];
-    return (L < 0 || L > p.max_pages * kPage) ? 0 : L;
+__device__ __forceinline__ int seq_cost(int L, int Hkv) {
+    return Hkv * (kCostTile * ((L + kTileKeys - 1) / kTileKeys) + kCostBlock);
 }
 
 struct Piece {
@@ -146,25 +152,27 @@ struct WorkIter {
     long long U, lo, hi, X;
     int b, g, L, ntc, C;
     int B, Hkv;
+    const long long *pre;   // shared: prefix sums of the sequences' work units
+    const int *lens;        // shared: clamped context lengths
 
-    __device__ void init(const TcParams &p, int group) {
-        B = p.B; Hkv = p.Hkv;
-        U = 0;
-        for (int i = 0; i < B; ++i)
-            U += (long long)Hkv * (kCostTile * ((clamp_len(p, i) + kTileKeys - 1) / kTileKeys) + kCostBlock);
+    __device__ void init(const TcParams &p, int group, const long long *pre_, const int *lens_) {
+        B = p.B; Hkv = p.Hkv; pre = pre_; lens = lens_;
+        U = pre[B];
         lo = (long long)group * U / p.n_groups;
         hi = (long long)(group + 1) * U / p.n_groups;
-        X = 0; b = 0; g = 0;
-        load(p);
-        while (b < B && X + (long long)Hkv * C <= lo) {   // skip sequences that end before lo
-            X += (long long)Hkv * C;
-            ++b;
-            if (b < B) load(p);
+        // the first sequence that ends after lo
+        int a = 0, z = B;
+        while (a < z) {
+            const int mid = (a + z) >> 1;
+            if (pre[mid + 1] > lo) z = mid; else a = mid + 1;
         }
+        b = a; g = 0;
+        X = (b < B) ? pre[b] : U;
+        load(p);
     }
-    __device__ void load(const TcParams &p) {
+    __device__ void load(const TcParams &) {
         if (b < B) {
-            L = clamp_len(p, b);
+            L = lens[b];
             ntc = (L + kTileKeys - 1) / kTileKeys;
             C = kCostTile * ntc + kCostBlock;
         }
@@ -285,7 +293,8 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&sv)[32], int col0, i
 
 // ------------------------------------------------------------------ the kernel
 //
-// Warps: 0 TMA producer; 1 QK issuer; 2 PV issuer; 3 idle; 4..11 softmax and epilogue
+// Warps: 0 TMA producer of Q and K; 1 QK issuer; 2 PV issuer; 3 TMA producer of V;
+// 4..11 softmax and epilogue
 // (two warps per TMEM lane quarter taking alternate tiles; at the end of a piece each
 // writes half of the O columns).
 
@@ -321,38 +330,72 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         sh.abort = 0;
         prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_kb); prefetch_tmap(&tm_vb);
-        for (int i = 0; i < p.B; ++i) {
-            const int L = p.ctx_len[i];
-            if (L < 0 || L > p.max_pages * kPage) { report_error(p.dev_err, TT_ERR_BOUNDS); break; }
+    }
+    // the sequence table: lengths loaded by all threads at once, prefix sums by warp 2
+    long long *seq_pre = reinterpret_cast<long long *>(sm + kOffSeqPre);
+    int *seq_len = reinterpret_cast<int *>(sm + kOffSeqLen);
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+        int L = p.ctx_len[i];
+        if (L < 0 || L > p.max_pages * kPage) {
+            report_error(p.dev_err, TT_ERR_BOUNDS);
+            L = 0;
         }
+        seq_len[i] = L;
     }
     if (warp == 1) { tmem_alloc(&sh.tmem_base, kTmemCols); tmem_relinquish(); }
+    __syncthreads();
+    if (warp == 2) {
+        long long carry = 0;
+        if (lane == 0) seq_pre[0] = 0;
+        for (int base = 0; base < p.B; base += 32) {
+            const int i = base + lane;
+            long long v = (i < p.B) ? (long long)seq_cost(seq_len[i], p.Hkv) : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (i < p.B) seq_pre[i + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
     WorkIter it;
-    it.init(p, group);
+    it.init(p, group, seq_pre, seq_len);
     const int S = p.S, G = p.G;
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 3) {
         regs_release();
-        // ================================================================ TMA producer
-        // The whole warp walks the work (page ids are fetched 32 at a time, one per lane);
-        // lane 0 issues the copies.
+        // ================================================================ TMA producers
+        // Warp 0 loads Q and K, warp 3 loads V, so that a K copy never waits behind the
+        // release of a V stage (they are freed by different products).  Each whole warp
+        // walks the work (page ids are fetched 32 at a time, one per lane); lane 0 issues
+        // the copies.
+        const bool is_v = warp == 3;
+        const CUtensorMap *tm_pool = is_v ? &tm_v : &tm_k;
+        const CUtensorMap *tm_blk = is_v ? &tm_vb : &tm_kb;
+        const int nst = is_v ? kVStages : kKStages;
+        uint64_t *full = is_v ? bar.v_full : bar.k_full;
+        uint64_t *empty = is_v ? bar.v_empty : bar.k_empty;
+        unsigned char *ring = sm + (is_v ? kOffV : kOffK);
         Piece pc;
         int qi = 0, t = 0;
         bool issued = false;
         while (it.next(p, pc)) {
-            if (!wait_bar(sh, &bar.q_empty, (qi & 1) ^ 1, p.dev_err)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bar.q_full, (uint32_t)kStage);
-                for (int dh = 0; dh < 2; ++dh)
-                    tma_load_3d(sm + kOffQ + dh * kHalf, &tm_q, &bar.q_full, 64 * dh, pc.g * G,
-                                pc.b * S + mt * (128 / G));
+            if (!is_v) {
+                if (!wait_bar(sh, &bar.q_empty, (qi & 1) ^ 1, p.dev_err)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar.q_full, (uint32_t)kStage);
+                    for (int dh = 0; dh < 2; ++dh)
+                        tma_load_3d(sm + kOffQ + dh * kHalf, &tm_q, &bar.q_full, 64 * dh, pc.g * G,
+                                    pc.b * S + mt * (128 / G));
+                }
+                issued = true;
             }
-            issued = true;
             bool ok = true;
             int my_page = 0;
             for (int i = pc.first; i < pc.last; ++i, ++t) {
@@ -374,43 +417,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int valid = tile_valid(pc, i, S);
                 const bool ctx = i < pc.ntc;
                 const bool two = ctx && valid > kPage;
-                const int kst = t % kKStages, vst = t % kVStages;
-                if (!wait_bar(sh, &bar.k_empty[kst], ((uint32_t)(t / kKStages) & 1) ^ 1, p.dev_err)) { ok = false; break; }
-                unsigned char *kd = sm + kOffK + kst * kStage;
-                unsigned char *vd = sm + kOffV + vst * kStage;
+                const int st = t % nst;
+                if (!wait_bar(sh, &empty[st], ((uint32_t)(t / nst) & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                unsigned char *dst = ring + st * kStage;
                 if (lane == 0) {
                     if (ctx) {
-                        mbar_arrive_expect_tx(&bar.k_full[kst], two ? 4 * 8192u : 2 * 8192u);
-                        tma_load_4d(kd, &tm_k, &bar.k_full[kst], 0, 0, pc.g, page0);
-                        tma_load_4d(kd + kHalf, &tm_k, &bar.k_full[kst], 64, 0, pc.g, page0);
+                        mbar_arrive_expect_tx(&full[st], two ? 4 * 8192u : 2 * 8192u);
+                        tma_load_4d(dst, tm_pool, &full[st], 0, 0, pc.g, page0);
+                        tma_load_4d(dst + kHalf, tm_pool, &full[st], 64, 0, pc.g, page0);
                         if (two) {
-                            tma_load_4d(kd + 8192, &tm_k, &bar.k_full[kst], 0, 0, pc.g, page1);
-                            tma_load_4d(kd + kHalf + 8192, &tm_k, &bar.k_full[kst], 64, 0, pc.g, page1);
+                            tma_load_4d(dst + 8192, tm_pool, &full[st], 0, 0, pc.g, page1);
+                            tma_load_4d(dst + kHalf + 8192, tm_pool, &full[st], 64, 0, pc.g, page1);
                         }
                     } else {
-                        mbar_arrive_expect_tx(&bar.k_full[kst], (uint32_t)(2 * S * 128));
-                        tma_load_3d(kd, &tm_kb, &bar.k_full[kst], 0, pc.g, pc.b * S);
-                        tma_load_3d(kd + kHalf, &tm_kb, &bar.k_full[kst], 64, pc.g, pc.b * S);
-                    }
-                }
-                if (!wait_bar(sh, &bar.v_empty[vst], ((uint32_t)(t / kVStages) & 1) ^ 1, p.dev_err)) {
-                    ok = false;
-                    ++t;   // the K copy of this tile is in flight: count it for the drain
-                    break;
-                }
-                if (lane == 0) {
-                    if (ctx) {
-                        mbar_arrive_expect_tx(&bar.v_full[vst], two ? 4 * 8192u : 2 * 8192u);
-                        tma_load_4d(vd, &tm_v, &bar.v_full[vst], 0, 0, pc.g, page0);
-                        tma_load_4d(vd + kHalf, &tm_v, &bar.v_full[vst], 64, 0, pc.g, page0);
-                        if (two) {
-                            tma_load_4d(vd + 8192, &tm_v, &bar.v_full[vst], 0, 0, pc.g, page1);
-                            tma_load_4d(vd + kHalf + 8192, &tm_v, &bar.v_full[vst], 64, 0, pc.g, page1);
-                        }
-                    } else {
-                        mbar_arrive_expect_tx(&bar.v_full[vst], (uint32_t)(2 * S * 128));
-                        tma_load_3d(vd, &tm_vb, &bar.v_full[vst], 0, pc.g, pc.b * S);
-                        tma_load_3d(vd + kHalf, &tm_vb, &bar.v_full[vst], 64, pc.g, pc.b * S);
+                        mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * S * 128));
+                        tma_load_3d(dst, tm_blk, &full[st], 0, pc.g, pc.b * S);
+                        tma_load_3d(dst + kHalf, tm_blk, &full[st], 64, pc.g, pc.b * S);
                     }
                 }
             }
@@ -420,10 +442,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // Drain: every copy issued must land before the CTA may exit.  The last copy into
         // a stage completes that stage's latest phase.
         if (issued) mbar_wait(&bar.q_full, (uint32_t)(qi - 1) & 1, kWaitLimit);
-        for (int k = 1; k <= kKStages && t - k >= 0; ++k)
-            mbar_wait(&bar.k_full[(t - k) % kKStages], (uint32_t)((t - k) / kKStages) & 1, kWaitLimit);
-        for (int k = 1; k <= kVStages && t - k >= 0; ++k)
-            mbar_wait(&bar.v_full[(t - k) % kVStages], (uint32_t)((t - k) / kVStages) & 1, kWaitLimit);
+        for (int k = 1; k <= nst && t - k >= 0; ++k)
+            mbar_wait(&full[(t - k) % nst], (uint32_t)((t - k) / nst) & 1, kWaitLimit);
         __syncwarp();
     } else if (warp == 1) {
         regs_release();
@@ -519,8 +539,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (elect_one()) mma_commit(&bar.done[1]);
         __syncwarp();
-    } else if (warp == 3) {
-        regs_release();   // idle warp of the role warpgroup
     } else {
         regs_acquire();
         // ================================================================ softmax / epilogue
@@ -708,63 +726,60 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.o_empty);
-                __threadfence();
+                // One thread publishes the whole group's partial: the group barrier orders
+                // every thread's stores before its release, the acquire half orders the
+                // merge's loads (of the other pieces) after it.
                 if (!group_sync(sh, k_grp, p.dev_err)) { ok = false; break; }
                 unsigned *ticket = p.tickets + (size_t)pc.sg * p.cps + mt;
                 if (threadIdx.x == 128) {
                     const unsigned n_here = (unsigned)(pc.last - pc.first);
-                    const unsigned before = atomicAdd(ticket, n_here);
+                    const unsigned before = atom_add_acq_rel_gpu(ticket, n_here);
                     sh.last = (before + n_here == (unsigned)(pc.ntc + 1));
                 }
                 if (!group_sync(sh, k_grp, p.dev_err)) { ok = false; break; }
                 if (sh.last) {
-                    __threadfence();
-                    // merge every piece of this segment's M tile, in group order
+                    // Merge every piece of this segment's M tile in group order: an online
+                    // rescale, so each piece costs one round trip (its maximum, sum and 64
+                    // output values are loaded together).
                     const long long U = it.U;
                     const int n = p.n_groups;
                     const int c_first = owner(pc.X, U, n);
                     const int c_last = owner(pc.X + (long long)kCostTile * pc.ntc, U, n);
-                    float M = -INFINITY;
+                    float M = -INFINITY, Lsum = 0.f;
+                    float acc[64];
+#pragma unroll
+                    for (int d = 0; d < 64; ++d) acc[d] = 0.f;
                     for (int c = c_first; c <= c_last; ++c) {
                         if (!owns_tile(c, pc.X, pc.ntc, U, n)) continue;
                         const float *sl = p.part + (long long)(c + pc.sg) * p.slot_floats;
-                        M = fmaxf(M, __ldcg(sl + (size_t)p.rows * kD + r));
-                    }
-                    float Lsum = 0.f;
-                    for (int c = c_first; c <= c_last; ++c) {
-                        if (!owns_tile(c, pc.X, pc.ntc, U, n)) continue;
-                        const float *sl = p.part + (long long)(c + pc.sg) * p.slot_floats;
-                        Lsum += fast_exp2(__ldcg(sl + (size_t)p.rows * kD + r) - M) *
-                                __ldcg(sl + (size_t)p.rows * kD + p.rows + r);
+                        const float4 *orw = reinterpret_cast<const float4 *>(sl + (size_t)r * kD + 64 * h);
+                        float4 v[16];
+#pragma unroll
+                        for (int d4 = 0; d4 < 16; ++d4) v[d4] = __ldcg(orw + d4);
+                        const float mc = __ldcg(sl + (size_t)p.rows * kD + r);
+                        const float lc = __ldcg(sl + (size_t)p.rows * kD + p.rows + r);
+                        const float Mn = fmaxf(M, mc);
+                        const float a = fast_exp2(M - Mn), w = fast_exp2(mc - Mn);
+                        Lsum = Lsum * a + lc * w;
+#pragma unroll
+                        for (int d4 = 0; d4 < 16; ++d4) {
+                            acc[4 * d4] = acc[4 * d4] * a + w * v[d4].x;
+                            acc[4 * d4 + 1] = acc[4 * d4 + 1] * a + w * v[d4].y;
+                            acc[4 * d4 + 2] = acc[4 * d4 + 2] * a + w * v[d4].z;
+                            acc[4 * d4 + 3] = acc[4 * d4 + 3] * a + w * v[d4].w;
+                        }
+                        M = Mn;
                     }
                     const float inv = 1.f / Lsum;
                     uint16_t *orow_out = p.out + (((size_t)pc.b * S + s_pos) * p.Hq + hq) * kD + 64 * h;
-                    for (int ch = 0; ch < 2; ++ch) {
-                        float acc[32];
 #pragma unroll
-                        for (int d = 0; d < 32; ++d) acc[d] = 0.f;
-                        for (int c = c_first; c <= c_last; ++c) {
-                            if (!owns_tile(c, pc.X, pc.ntc, U, n)) continue;
-                            const float *sl = p.part + (long long)(c + pc.sg) * p.slot_floats;
-                            const float w = fast_exp2(__ldcg(sl + (size_t)p.rows * kD + r) - M);
-                            const float4 *orw =
-                                reinterpret_cast<const float4 *>(sl + (size_t)r * kD + 64 * h + 32 * ch);
-#pragma unroll
-                            for (int d4 = 0; d4 < 8; ++d4) {
-                                const float4 v = __ldcg(orw + d4);
-                                acc[4 * d4] += w * v.x; acc[4 * d4 + 1] += w * v.y;
-                                acc[4 * d4 + 2] += w * v.z; acc[4 * d4 + 3] += w * v.w;
-                            }
-                        }
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint4 w;
-                            w.x = pack_bf16(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
-                            w.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
-                            w.z = pack_bf16(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
-                            w.w = pack_bf16(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
-                            *reinterpret_cast<uint4 *>(orow_out + 32 * ch + 8 * k) = w;
-                        }
+                    for (int k = 0; k < 8; ++k) {
+                        uint4 w;
+                        w.x = pack_bf16(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
+                        w.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+                        w.z = pack_bf16(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+                        w.w = pack_bf16(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+                        *reinterpret_cast<uint4 *>(orow_out + 8 * k) = w;
                     }
                     if (p.lse && h == 0)
                         p.lse[((size_t)pc.b * p.Hq + hq) * S + s_pos] = (M + __log2f(Lsum)) * kLn2;
@@ -831,25 +846,29 @@ bool attn_tc_supported(int S, int Hq, int Hkv, int D, int page_size, tt_dtype dt
 size_t attn_tc_ws_bytes(int B, int S, int Hq, int Hkv, int D) {
     const size_t rows = (size_t)rows_of(S, Hq, Hkv);
     const size_t slot = (rows * D + 2 * rows) * sizeof(float);
-    const size_t nseg = (size_t)B * Hkv;
+    const size_t nseg = (size_t)(B < kSeqMax ? B : kSeqMax) * Hkv;   // one launch's segments
     return align_up(2 * nseg * sizeof(unsigned), 256) + (kMaxCtas + nseg) * slot;
 }
 
-tt_status launch_attn_tc(const AttnArgs &a) {
+namespace {
+
+// One launch over sequences [b0, b0 + nb) (nb <= kSeqMax): every per-sequence pointer is
+// offset to b0, the pools are shared.
+tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     const tt_kv_cache &c = *a.ctx;
-    if (c.num_pages < 1) return launch_attn_simt(a);      // no pool to map: nothing paged to read
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return TT_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TT_ERR_CUDA;
+    const size_t qrow = (size_t)a.Hq * kD, kvrow = (size_t)a.Hkv * kD;
+    const uint16_t *q = static_cast<const uint16_t *>(a.q) + (size_t)b0 * a.S * qrow;
+    const uint16_t *k_blk = static_cast<const uint16_t *>(a.k_blk) + (size_t)b0 * a.S * kvrow;
+    const uint16_t *v_blk = static_cast<const uint16_t *>(a.v_blk) + (size_t)b0 * a.S * kvrow;
     const int G = a.Hq / a.Hkv;
     const int rows = G * a.S;
     const int cps = rows / 128;   // CTAs per segment, one per 128-row M tile
     CUtensorMap mq, mk, mv, mkb, mvb;
     {
-        const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)a.B * a.S};
+        const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)nb * a.S};
         const uint64_t str[2] = {(uint64_t)kD * 2, (uint64_t)a.Hq * kD * 2};
         const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(128 / G)};
-        if (!make_map(&mq, a.q, 3, dims, str, box)) return TT_ERR_CUDA;
+        if (!make_map(&mq, q, 3, dims, str, box)) return TT_ERR_CUDA;
     }
     {
         const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)kPage, (uint64_t)a.Hkv, (uint64_t)c.num_pages};
@@ -859,26 +878,26 @@ tt_status launch_attn_tc(const AttnArgs &a) {
         if (!make_map(&mv, c.v_pool, 4, dims, str, box)) return TT_ERR_CUDA;
     }
     {
-        const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.B * a.S};
+        const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)nb * a.S};
         const uint64_t str[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};
         const uint32_t box[3] = {64, 1, (uint32_t)a.S};
-        if (!make_map(&mkb, a.k_blk, 3, dims, str, box)) return TT_ERR_CUDA;
-        if (!make_map(&mvb, a.v_blk, 3, dims, str, box)) return TT_ERR_CUDA;
+        if (!make_map(&mkb, k_blk, 3, dims, str, box)) return TT_ERR_CUDA;
+        if (!make_map(&mvb, v_blk, 3, dims, str, box)) return TT_ERR_CUDA;
     }
     TcParams p;
-    p.page_table = c.page_table;
-    p.ctx_len = c.ctx_len;
+    p.page_table = c.page_table + (size_t)b0 * c.max_pages_per_seq;
+    p.ctx_len = c.ctx_len + b0;
     p.num_pages = c.num_pages;
     p.max_pages = c.max_pages_per_seq;
-    p.out = static_cast<uint16_t *>(a.out);
-    p.lse = a.lse;
-    p.B = a.B; p.S = a.S; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rows = rows; p.cps = cps;
+    p.out = static_cast<uint16_t *>(a.out) + (size_t)b0 * a.S * qrow;
+    p.lse = a.lse ? a.lse + (size_t)b0 * a.Hq * a.S : nullptr;
+    p.B = nb; p.S = a.S; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rows = rows; p.cps = cps;
     p.scale_log2 = a.sm_scale * kLog2e;
     int n = a.max_ctas > 0 ? a.max_ctas : sms;
     if (n > kMaxCtas) n = kMaxCtas;
     const int n_groups = n / cps > 0 ? n / cps : 1;
     p.n_groups = n_groups;
-    const size_t nseg = (size_t)a.B * a.Hkv;
+    const size_t nseg = (size_t)nb * a.Hkv;
     p.tickets = static_cast<unsigned *>(a.ws);
     p.part = reinterpret_cast<float *>(static_cast<char *>(a.ws) + align_up(2 * nseg * sizeof(unsigned), 256));
     p.slot_floats = (long long)rows * kD + 2LL * rows;
@@ -888,6 +907,22 @@ tt_status launch_attn_tc(const AttnArgs &a) {
         return TT_ERR_CUDA;
     attn_tc_kernel<<<n_groups * cps, 384, kSmemBytes, a.stream>>>(mq, mk, mv, mkb, mvb, p);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+}  // namespace
+
+// Batches above the kernel's sequence table run as consecutive launches on the stream;
+// they share the workspace, which each launch leaves as it found it (tickets zero).
+tt_status launch_attn_tc(const AttnArgs &a) {
+    if (a.ctx->num_pages < 1) return launch_attn_simt(a);   // no pool to map: nothing paged to read
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TT_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return TT_ERR_CUDA;
+    for (int b0 = 0; b0 < a.B; b0 += kSeqMax) {
+        const tt_status st = launch_chunk(a, b0, a.B - b0 < kSeqMax ? a.B - b0 : kSeqMax, sms);
+        if (st != TT_OK) return st;
+    }
+    return TT_OK;
 }
 
 }  // namespace tt

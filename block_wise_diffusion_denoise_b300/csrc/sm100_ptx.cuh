@@ -213,5 +213,14 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
+// Fetch-and-add with acquire-release semantics at GPU scope: releases the calling
+// thread's (and, after a CTA barrier, its block's) earlier writes and acquires the writes
+// released by earlier adds to the same word.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *ptr, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 }  // namespace sm100
 }  // namespace tt
