@@ -615,14 +615,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                     tc_fence_after();
                     const float alpha = moved ? fast_exp2(m_prev - m_t) : 1.f;
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t o[32];
-                        const uint32_t ocol = tmem + lane_off + kColO + 32 * ch;
-                        tmem_ld32(ocol, o);
+                    // 16 columns at a time: the tile's scores are live in registers meanwhile
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t o[16];
+                        const uint32_t ocol = tmem + lane_off + kColO + 16 * ch;
+                        tmem_ld16(ocol, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st32(ocol, o);
+                        for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st16(ocol, o);
                         tmem_wait_st();   // o is reused by the next chunk
                     }
                 }

@@ -12,9 +12,12 @@
 // (vocabulary chunk, position, sequence); each CTA brings one 32 KB chunk of one
 // row into shared memory with four bulk copies (cp.async.bulk, one mbarrier per
 // 8 KB piece) issued before any arithmetic, so up to six CTAs per SM keep about
-// 190 KB in flight with few registers.  Threads fold each piece into an online
-// (max, sum of exp relative to the max, first argmax) state, the CTA merges the
-// states in a fixed order and writes one partial.  The last CTA of a sequence to
+// 190 KB in flight with few registers.  Each thread makes two passes over its
+// vectors of a piece in shared memory -- the maximum (packed bf16 pairs, exact)
+// with the first vector holding it, then the sum of exponentials relative to
+// that maximum -- and merges the piece into a running (max, sum, first argmax)
+// state; the CTA merges the threads' states in a fixed order and writes one
+// partial.  The last CTA of a sequence to
 // finish (atomic ticket, no waiting) merges the partials of the sequence's rows
 // and applies the commit rules.  Locked rows cost one byte read.
 
@@ -126,6 +129,46 @@ __device__ __forceinline__ void fold(const float *x, int e0, float &m, float &z,
     for (int j = 0; j < EPV; ++j) z += fast_exp2(fmaf(x[j], kLog2e, -mc));
 }
 
+// Largest element of one 16-byte vector.  bf16: a packed pairwise maximum (exact in
+// bf16) and one scalar compare; fp32: a compare tree.
+template <typename T> __device__ __forceinline__ float vec_max(const uint4 &u);
+template <> __device__ __forceinline__ float vec_max<uint16_t>(const uint4 &u) {
+    uint32_t a, b, c;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(u.x), "r"(u.y));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(u.z), "r"(u.w));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(a), "r"(b));
+    return fmaxf(bf16_lo(c), bf16_hi(c));
+}
+template <> __device__ __forceinline__ float vec_max<float>(const uint4 &u) {
+    return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                 fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+}
+
+// Sum of 2^(x*log2e - mc) over one vector, in two independent partial sums.
+template <typename T>
+__device__ __forceinline__ void vec_expsum(const uint4 &u, float mc, float &z0, float &z1) {
+    constexpr int EPV = Vec<T>::kElems;
+    float x[EPV];
+    unpack<T>(u, x);
+#pragma unroll
+    for (int j = 0; j < EPV; j += 2) {
+        z0 += fast_exp2(fmaf(x[j], kLog2e, -mc));
+        z1 += fast_exp2(fmaf(x[j + 1], kLog2e, -mc));
+    }
+}
+
+// First position in the vector holding the value mx (which it holds).
+template <typename T>
+__device__ __forceinline__ int vec_first(const uint4 &u, float mx) {
+    constexpr int EPV = Vec<T>::kElems;
+    float x[EPV];
+    unpack<T>(u, x);
+    int j0 = EPV - 1;
+#pragma unroll
+    for (int j = EPV - 1; j >= 0; --j) j0 = (x[j] == mx) ? j : j0;
+    return j0;
+}
+
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) {
     constexpr int EPV = Vec<T>::kElems;               // elements per 16-byte vector
@@ -169,12 +212,23 @@ __global__ void __launch_bounds__(kThreads) unmask_kernel(const UnmaskParams p) 
                     timed_out = true;
                     break;
                 }
+                // Two passes over the piece in shared memory: this thread's maximum and
+                // the first of its vectors that holds it, then the sum of exponentials
+                // relative to that maximum; merged into the running state.
                 const int nv = pb / 16;
                 const uint4 *pv = buf + k * (kPieceBytes / 16);
+                float pm = -INFINITY;
+                int pvi = -1;
                 for (int v = tid; v < nv; v += kThreads) {
-                    float x[EPV];
-                    unpack<T>(pv[v], x);
-                    fold<EPV>(x, c0 + (k * (kPieceBytes / 16) + v) * EPV, m, z, a);
+                    const float vm = vec_max<T>(pv[v]);
+                    if (vm > pm) { pm = vm; pvi = v; }
+                }
+                if (pvi >= 0) {
+                    const float mc = pm * kLog2e;
+                    float z0 = 0.f, z1 = 0.f;
+                    for (int v = tid; v < nv; v += kThreads) vec_expsum<T>(pv[v], mc, z0, z1);
+                    const int pa = c0 + (k * (kPieceBytes / 16) + pvi) * EPV + vec_first<T>(pv[pvi], pm);
+                    merge(m, z, a, pm, z0 + z1, pa);
                 }
             }
             if (timed_out) {
