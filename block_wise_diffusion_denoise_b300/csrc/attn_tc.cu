@@ -64,8 +64,8 @@ using namespace sm100;
 constexpr int kD = 128;                  // head dim
 constexpr int kPage = 64;                // tokens per page
 constexpr int kTileKeys = 128;           // keys per context tile (two pages)
-constexpr int kKStages = 2;              // K ring depth
-constexpr int kVStages = 3;              // V ring depth
+constexpr int kKStages = 3;              // K ring depth (K is needed first: QK starts a tile)
+constexpr int kVStages = 2;              // V ring depth (V is needed last, after the softmax)
 constexpr int kMaxCtas = 296;            // upper bound of the persistent grid (sizes the workspace)
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -255,40 +255,60 @@ __device__ __forceinline__ int tile_valid(const Piece &pc, int i, int S) {
     return i < pc.ntc ? min(kTileKeys, pc.L - kTileKeys * i) : S;
 }
 
-// exp2 of 32 scores of a row -> 16 packed bf16 pairs; columns at or past `valid` give 0.
-template <bool kMasked>
-__device__ __forceinline__ float softmax_chunk(const uint32_t (&sv)[32], int col0, int valid, float c2, float m,
-                                               uint32_t (&pw)[16]) {
-    float sum0 = 0.f, sum1 = 0.f;
+// Scores at columns at or past `valid` become -inf (only the last context tile of a
+// segment and the block tile are partial), so one code path serves every tile.
+__device__ __forceinline__ void mask_scores(uint32_t (&sv)[32], int col0, int valid) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        float a = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c2, -m));
-        float b = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c2, -m));
-        if (kMasked) {
-            a = (col0 + 2 * k < valid) ? a : 0.f;
-            b = (col0 + 2 * k + 1 < valid) ? b : 0.f;
-        }
-        sum0 += a;
-        sum1 += b;
-        pw[k] = pack_bf16(a, b);
-    }
-    return sum0 + sum1;
+    for (int k = 0; k < 32; ++k)
+        if (col0 + k >= valid) sv[k] = 0xff800000u;
 }
 
-template <bool kMasked>
-__device__ __forceinline__ float chunk_max(const uint32_t (&sv)[32], int col0, int valid) {
-    float m0 = -INFINITY, m1 = -INFINITY;
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Largest of 32 scores (two independent three-input chains).
+__device__ __forceinline__ float chunk_max(const uint32_t (&sv)[32]) {
+    float m0 = max3f(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+    float m1 = max3f(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
+#pragma unroll
+    for (int k = 6; k < 30; k += 4) {
+        m0 = max3f(m0, __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
+        m1 = max3f(m1, __uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3]));
+    }
+    return max3f(m0, m1, fmaxf(__uint_as_float(sv[30]), __uint_as_float(sv[31])));
+}
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// exp2(s * c - m) of 32 scores -> 16 packed bf16 pairs and their sum; the scale and the
+// subtraction run as paired fp32 FMAs, the sums as paired adds.  cx2 = (c, c), nmx2 = (-m, -m).
+__device__ __forceinline__ float softmax_chunk(const uint32_t (&sv)[32], uint64_t cx2, uint64_t nmx2,
+                                               uint32_t (&pw)[16]) {
+    uint64_t acc0 = 0, acc1 = 0;   // (+0, +0)
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        float a = __uint_as_float(sv[2 * k]), b = __uint_as_float(sv[2 * k + 1]);
-        if (kMasked) {
-            a = (col0 + 2 * k < valid) ? a : -INFINITY;
-            b = (col0 + 2 * k + 1 < valid) ? b : -INFINITY;
-        }
-        m0 = fmaxf(m0, a);
-        m1 = fmaxf(m1, b);
+        uint64_t y;
+        asm("fma.rn.f32x2 %0, %1, %2, %3;"
+            : "=l"(y)
+            : "l"(f32x2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]))), "l"(cx2), "l"(nmx2));
+        float y0, y1;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(y));
+        const float a = fast_exp2(y0), b = fast_exp2(y1);
+        if (k & 1) asm("add.f32x2 %0, %0, %1;" : "+l"(acc1) : "l"(f32x2(a, b)));
+        else asm("add.f32x2 %0, %0, %1;" : "+l"(acc0) : "l"(f32x2(a, b)));
+        pw[k] = pack_bf16(a, b);
     }
-    return fmaxf(m0, m1);
+    asm("add.f32x2 %0, %0, %1;" : "+l"(acc0) : "l"(acc1));
+    float s0, s1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(acc0));
+    return s0 + s1;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -571,23 +591,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // maximum, and S released to the next QK product right away
                 uint32_t a0[32], a1[32], a2[32], a3[32];
                 tmem_ld32(scol, a0);
-                if (valid > 32) tmem_ld32(scol + 32, a1);
-                if (valid > 64) tmem_ld32(scol + 64, a2);
-                if (valid > 96) tmem_ld32(scol + 96, a3);
+                tmem_ld32(scol + 32, a1);
+                tmem_ld32(scol + 64, a2);
+                tmem_ld32(scol + 96, a3);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
-                float mx;
-                if (valid == kTileKeys) {
-                    mx = fmaxf(fmaxf(chunk_max<false>(a0, 0, valid), chunk_max<false>(a1, 32, valid)),
-                               fmaxf(chunk_max<false>(a2, 64, valid), chunk_max<false>(a3, 96, valid)));
-                } else {
-                    mx = chunk_max<true>(a0, 0, valid);
-                    if (valid > 32) mx = fmaxf(mx, chunk_max<true>(a1, 32, valid));
-                    if (valid > 64) mx = fmaxf(mx, chunk_max<true>(a2, 64, valid));
-                    if (valid > 96) mx = fmaxf(mx, chunk_max<true>(a3, 96, valid));
+                if (valid < kTileKeys) {   // warp-uniform
+                    mask_scores(a0, 0, valid);
+                    mask_scores(a1, 32, valid);
+                    mask_scores(a2, 64, valid);
+                    mask_scores(a3, 96, valid);
                 }
+                const float mx = fmaxf(fmaxf(chunk_max(a0), chunk_max(a1)), fmaxf(chunk_max(a2), chunk_max(a3)));
                 // ---- the running maximum: the previous tile's (from the partner), raised when
                 // this tile's maximum exceeds it by more than 2^8
                 float m_prev = -INFINITY;
@@ -635,33 +652,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // registers at issue; tcgen05.wait::st below orders the TMEM writes before the PV
                 // product)
                 const uint32_t pcolt = tmem + lane_off + kColP + 64 * sb;
-                float psum;
+                const uint64_t cx2 = f32x2(c2, c2), nmx2 = f32x2(-m_t, -m_t);
                 uint32_t pw[16];
-                if (valid == kTileKeys) {
-                    psum = softmax_chunk<false>(a0, 0, valid, c2, m_t, pw);
-                    tmem_st16(pcolt, pw);
-                    psum += softmax_chunk<false>(a1, 32, valid, c2, m_t, pw);
-                    tmem_st16(pcolt + 16, pw);
-                    psum += softmax_chunk<false>(a2, 64, valid, c2, m_t, pw);
-                    tmem_st16(pcolt + 32, pw);
-                    psum += softmax_chunk<false>(a3, 96, valid, c2, m_t, pw);
-                    tmem_st16(pcolt + 48, pw);
-                } else {
-                    psum = softmax_chunk<true>(a0, 0, valid, c2, m_t, pw);
-                    tmem_st16(pcolt, pw);
-                    if (valid > 32) {
-                        psum += softmax_chunk<true>(a1, 32, valid, c2, m_t, pw);
-                        tmem_st16(pcolt + 16, pw);
-                    }
-                    if (valid > 64) {
-                        psum += softmax_chunk<true>(a2, 64, valid, c2, m_t, pw);
-                        tmem_st16(pcolt + 32, pw);
-                    }
-                    if (valid > 96) {
-                        psum += softmax_chunk<true>(a3, 96, valid, c2, m_t, pw);
-                        tmem_st16(pcolt + 48, pw);
-                    }
-                }
+                float psum = softmax_chunk(a0, cx2, nmx2, pw);
+                tmem_st16(pcolt, pw);
+                psum += softmax_chunk(a1, cx2, nmx2, pw);
+                tmem_st16(pcolt + 16, pw);
+                psum += softmax_chunk(a2, cx2, nmx2, pw);
+                tmem_st16(pcolt + 32, pw);
+                psum += softmax_chunk(a3, cx2, nmx2, pw);
+                tmem_st16(pcolt + 48, pw);
                 tmem_wait_st();
                 l += psum;
                 tc_fence_before();
@@ -707,16 +707,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.o_empty);
             } else {
-                // partial: unnormalised O, the row maximum used (log2 units) and the row sum
+                // partial: unnormalised O, the row maximum used (log2 units) and the row sum.
+                // O is stored as [column / 4][row][4] so that the lanes (consecutive rows)
+                // write, and later read, consecutive 16-byte pieces.
                 float *slot = p.part + (long long)(group + pc.sg) * p.slot_floats;
-                float *orow = slot + (size_t)r * kD + 64 * h;
+                float4 *ocol4 = reinterpret_cast<float4 *>(slot) + r;
                 for (int ch = 0; ch < 2; ++ch) {
                     uint32_t o[32];
                     tmem_ld32(tmem + lane_off + kColO + 64 * h + 32 * ch, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        __stcg(reinterpret_cast<float4 *>(orow + 32 * ch + 4 * k),
+                        __stcg(ocol4 + (size_t)(16 * h + 8 * ch + k) * p.rows,
                                make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
                                            __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3])));
                 }
@@ -753,10 +755,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int c = c_first; c <= c_last; ++c) {
                         if (!owns_tile(c, pc.X, pc.ntc, U, n)) continue;
                         const float *sl = p.part + (long long)(c + pc.sg) * p.slot_floats;
-                        const float4 *orw = reinterpret_cast<const float4 *>(sl + (size_t)r * kD + 64 * h);
+                        const float4 *orw = reinterpret_cast<const float4 *>(sl) + (size_t)16 * h * p.rows + r;
                         float4 v[16];
 #pragma unroll
-                        for (int d4 = 0; d4 < 16; ++d4) v[d4] = __ldcg(orw + d4);
+                        for (int d4 = 0; d4 < 16; ++d4) v[d4] = __ldcg(orw + (size_t)d4 * p.rows);
                         const float mc = __ldcg(sl + (size_t)p.rows * kD + r);
                         const float lc = __ldcg(sl + (size_t)p.rows * kD + p.rows + r);
                         const float Mn = fmaxf(M, mc);
