@@ -441,6 +441,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!wait_bar(sh, &empty[st], ((uint32_t)(t / nst) & 1) ^ 1, p.dev_err)) { ok = false; break; }
                 unsigned char *dst = ring + st * kStage;
                 if (lane == 0) {
+                    if (ctx && !is_v) {
+                        // The same tile's V pages are needed two tile periods later than its
+                        // K, behind a shallower ring: start them towards L2 now.
+                        tma_prefetch_4d(&tm_v, 0, 0, pc.g, page0);
+                        tma_prefetch_4d(&tm_v, 64, 0, pc.g, page0);
+                        if (two) {
+                            tma_prefetch_4d(&tm_v, 0, 0, pc.g, page1);
+                            tma_prefetch_4d(&tm_v, 64, 0, pc.g, page1);
+                        }
+                    }
                     if (ctx) {
                         mbar_arrive_expect_tx(&full[st], two ? 4 * 8192u : 2 * 8192u);
                         tma_load_4d(dst, tm_pool, &full[st], 0, 0, pc.g, page0);
