@@ -69,7 +69,16 @@ constexpr int kVStages = 2;              // V ring depth (V is needed last, afte
 constexpr int kMaxCtas = 296;            // upper bound of the persistent grid (sizes the workspace)
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr int kCostTile = 8, kCostBlock = 1;
+// Work units of the stream-K split: a context tile costs kCostTile, the block tile
+// kCostBlock (its MMAs are short but its softmax is a full tile's), and every segment
+// carries kCostSeg up front for what a piece boundary costs (Q load, pipeline refill,
+// epilogue and, for split segments, the merge).
+constexpr int kCostTile = 8, kCostBlock = 6, kCostSeg = 24;
+// Splitting a segment between groups costs about this many units more than it saves
+// (a second piece boundary, the partial write and the merge): when every group can take
+// a whole segment and the longest one is within this margin of the even split, each
+// group takes one whole segment instead.
+constexpr int kCostSplit = 80;
 
 // Shared memory (offsets from a 1024-byte aligned base).  Every 128-row operand is
 // stored as two 128-byte-swizzled halves of 64 columns (d 0..63 and d 64..127).
@@ -130,12 +139,13 @@ struct Shared {
     uint32_t tmem_base;
     int abort;
     int last;
+    int max_len;           // longest context of the launch
 };
 
 // ------------------------------------------------------------------ work partition
 
 __device__ __forceinline__ int seq_cost(int L, int Hkv) {
-    return Hkv * (kCostTile * ((L + kTileKeys - 1) / kTileKeys) + kCostBlock);
+    return Hkv * (kCostSeg + kCostTile * ((L + kTileKeys - 1) / kTileKeys) + kCostBlock);
 }
 
 struct Piece {
@@ -147,7 +157,7 @@ struct Piece {
 };
 
 // Walks the pieces of one CTA group's cost range [lo, hi).  Tile i of a segment that
-// starts at unit X starts at unit X + kCostTile * i; the block tile (i = ntc) costs 1.
+// starts at unit X starts at unit X + kCostSeg + kCostTile * i (the block tile is i = ntc).
 struct WorkIter {
     long long U, lo, hi, X;
     int b, g, L, ntc, C;
@@ -155,11 +165,24 @@ struct WorkIter {
     const long long *pre;   // shared: prefix sums of the sequences' work units
     const int *lens;        // shared: clamped context lengths
 
-    __device__ void init(const TcParams &p, int group, const long long *pre_, const int *lens_) {
+    __device__ void init(const TcParams &p, int group, const long long *pre_, const int *lens_, int max_len) {
         B = p.B; Hkv = p.Hkv; pre = pre_; lens = lens_;
         U = pre[B];
-        lo = (long long)group * U / p.n_groups;
-        hi = (long long)(group + 1) * U / p.n_groups;
+        const long long nseg = (long long)B * Hkv;
+        const long long max_seg = seq_cost(max_len, 1);
+        if (nseg <= p.n_groups && max_seg <= U / p.n_groups + kCostSplit) {
+            // one whole segment per group: the range of segment `group` exactly
+            if (group < nseg) {
+                const int sb = (int)(group / Hkv), sg = (int)(group % Hkv);
+                lo = pre[sb] + (long long)sg * seq_cost(lens[sb], 1);
+                hi = lo + seq_cost(lens[sb], 1);
+            } else {
+                lo = hi = U;
+            }
+        } else {
+            lo = (long long)group * U / p.n_groups;
+            hi = (long long)(group + 1) * U / p.n_groups;
+        }
         // the first sequence that ends after lo
         int a = 0, z = B;
         while (a < z) {
@@ -174,13 +197,14 @@ struct WorkIter {
         if (b < B) {
             L = lens[b];
             ntc = (L + kTileKeys - 1) / kTileKeys;
-            C = kCostTile * ntc + kCostBlock;
+            C = kCostSeg + kCostTile * ntc + kCostBlock;
         }
     }
     __device__ bool next(const TcParams &p, Piece &pc) {
         while (b < B && X < hi) {
-            const long long first = (lo > X) ? (lo - X + kCostTile - 1) / kCostTile : 0;
-            long long last = (hi - X + kCostTile - 1) / kCostTile;
+            const long long T0 = X + kCostSeg;   // unit of tile 0
+            const long long first = (lo > T0) ? (lo - T0 + kCostTile - 1) / kCostTile : 0;
+            long long last = (hi > T0) ? (hi - T0 + kCostTile - 1) / kCostTile : 0;
             if (last > ntc + 1) last = ntc + 1;
             const bool have = first < last;
             if (have) {
@@ -209,8 +233,9 @@ __device__ __forceinline__ int owner(long long u, long long U, int n) {
 // Does group c own at least one tile of the segment starting at unit X with ntc context tiles?
 __device__ __forceinline__ bool owns_tile(int c, long long X, int ntc, long long U, int n) {
     const long long lo_c = range_lo(c, U, n), hi_c = range_lo(c + 1, U, n);
-    const long long i0 = (lo_c > X) ? (lo_c - X + kCostTile - 1) / kCostTile : 0;
-    return i0 <= ntc && X + kCostTile * i0 < hi_c;
+    const long long T0 = X + kCostSeg;
+    const long long i0 = (lo_c > T0) ? (lo_c - T0 + kCostTile - 1) / kCostTile : 0;
+    return i0 <= ntc && T0 + kCostTile * i0 < hi_c;
 }
 
 // ------------------------------------------------------------------ helpers
@@ -249,6 +274,18 @@ __device__ __forceinline__ bool elect_one() {
     uint32_t pred;
     asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
     return pred != 0;
+}
+
+// Physical page of logical page pg of the piece's sequence (0 past the context; an id
+// outside the pool is reported and replaced by 0 so that no copy leaves the pool).
+__device__ __forceinline__ int page_id(const TcParams &p, const Piece &pc, int pg) {
+    if (pg * kPage >= pc.L) return 0;
+    const int id = p.page_table[(size_t)pc.b * p.max_pages + pg];
+    if (id < 0 || id >= p.num_pages) {
+        report_error(p.dev_err, TT_ERR_BOUNDS);
+        return 0;
+    }
+    return id;
 }
 
 __device__ __forceinline__ int tile_valid(const Piece &pc, int i, int S) {
@@ -366,10 +403,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     if (warp == 2) {
         long long carry = 0;
+        int mlen = 0;
         if (lane == 0) seq_pre[0] = 0;
         for (int base = 0; base < p.B; base += 32) {
             const int i = base + lane;
             long long v = (i < p.B) ? (long long)seq_cost(seq_len[i], p.Hkv) : 0;
+            if (i < p.B) mlen = max(mlen, seq_len[i]);
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const long long u = __shfl_up_sync(0xffffffffu, v, o);
@@ -378,6 +417,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (i < p.B) seq_pre[i + 1] = carry + v;
             carry += __shfl_sync(0xffffffffu, v, 31);
         }
+        mlen = __reduce_max_sync(0xffffffffu, mlen);
+        if (lane == 0) sh.max_len = mlen;
     }
     tc_fence_before();
     __syncthreads();
@@ -385,7 +426,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t tmem = sh.tmem_base;
 
     WorkIter it;
-    it.init(p, group, seq_pre, seq_len);
+    it.init(p, group, seq_pre, seq_len, sh.max_len);
     const int S = p.S, G = p.G;
 
     if (warp == 0 || warp == 3) {
@@ -421,17 +462,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int i = pc.first; i < pc.last; ++i, ++t) {
                 // page ids of tiles [i, i + 16): lane l holds page 2i + l of the sequence
                 const int rel = i - pc.first;
-                if ((rel & 15) == 0) {
-                    const int pg = 2 * i + lane;
-                    my_page = 0;
-                    if (pg * kPage < pc.L) {
-                        my_page = p.page_table[(size_t)pc.b * p.max_pages + pg];
-                        if (my_page < 0 || my_page >= p.num_pages) {
-                            report_error(p.dev_err, TT_ERR_BOUNDS);
-                            my_page = 0;
-                        }
-                    }
-                }
+                if ((rel & 15) == 0) my_page = page_id(p, pc, 2 * i + lane);
                 const int page0 = __shfl_sync(0xffffffffu, my_page, (2 * rel) & 31);
                 const int page1 = __shfl_sync(0xffffffffu, my_page, (2 * rel + 1) & 31);
                 const int valid = tile_valid(pc, i, S);
@@ -756,8 +787,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // output values are loaded together).
                     const long long U = it.U;
                     const int n = p.n_groups;
-                    const int c_first = owner(pc.X, U, n);
-                    const int c_last = owner(pc.X + (long long)kCostTile * pc.ntc, U, n);
+                    const int c_first = owner(pc.X + kCostSeg, U, n);
+                    const int c_last = owner(pc.X + kCostSeg + (long long)kCostTile * pc.ntc, U, n);
                     float M = -INFINITY, Lsum = 0.f;
                     float acc[64];
 #pragma unroll
