@@ -185,7 +185,7 @@ TT_API tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int
                     tt_stream_t stream);
 
 /* Largest scratch, in bytes, that tt_unmask_noalloc can use (its file-scope device array). */
-#define TT_UNMASK_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+#define TT_UNMASK_NOALLOC_SCRATCH_BYTES (1024u * 1024u)
 
 /* tt_unmask for callers that cannot allocate device memory.  (The pages have no
  * counterpart of this call; it exists for deployment.)
@@ -205,7 +205,7 @@ TT_API tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int
  *    device, with that device current); make that first call before any stream
  *    capture.
  *  - A shape whose scratch would exceed the array returns TT_ERR_CAPACITY before
- *    anything is launched (tt_unmask_workspace_size gives the need; about 64 KB
+ *    anything is launched (tt_unmask_workspace_size gives the need; about 82 KB
  *    for 32 sequences x 16 positions x 131072 bf16 logits).
  *  - Every call shares the one array and it keeps the last call's contents; the
  *    counters that must start at zero are cleared on the stream before each
