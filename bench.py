@@ -53,6 +53,35 @@ def parse():
 
 # --------------------------------------------------------------------------- algorithmic cost
 
+CSRC = os.path.join(ROOT, "block_wise_diffusion_denoise_b300", "csrc")
+PROFILED = {   # kernel -> (summary under profiles/, the sources its counters were taken from)
+    "attention": ("attention_ctx8k.md", ("attn_tc.cu", "sm100_ptx.cuh", "tt_common.cuh")),
+    "unmask": ("unmask_ctx8k.md", ("unmask.cu", "sm100_ptx.cuh", "tt_common.cuh")),
+}
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or None when the
+    summary is for another workload or the kernel's sources have changed since the capture."""
+    import hashlib
+    name, files = PROFILED[kernel]
+    path = os.path.join(ROOT, "profiles", name)
+    if workload != "ctx8k" or not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.split(":", 1)[0] in ("kernel_sources_sha256", "traffic_bytes_per_launch"):
+            k, v = line.split(":", 1)
+            fields[k] = v.split()[0]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("kernel_sources_sha256") != h.hexdigest()[:16] or "traffic_bytes_per_launch" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
 def attn_bytes(cfg, lens) -> float:
     """Bytes a perfect attention kernel moves: context K/V once, q, block K/V and the output."""
     elem = 2 if cfg.dtype == "bf16" else 4
@@ -486,12 +515,15 @@ def run_ours(a, cfg):
                          "unit": "GB/s", "frac": attn_gbs / hbm, "peak_source": src,
                          "algorithmic_bytes_per_launch": ab, "avg_launch_us": attn_ms * 1e3,
                          "tensor_tflops": attn_tfs, "tensor_frac": attn_tfs / tc,
-                         "traffic": None},
+                         "traffic": profiled_traffic("attention", cfg.name),
+                         "traffic_source": "profiles/attention_ctx8k.md (ncu dram__bytes_read.sum + "
+                                           "dram__bytes_write.sum, one launch)"},
             "kernels": {
                 "attention": {"us": attn_ms * 1e3, "gbs": attn_gbs, "hbm_frac": attn_gbs / hbm,
                               "roofline_us": max(ab / (hbm * 1e9), af / (tc * 1e12)) * 1e6},
                 "unmask": {"us": unmask_ms * 1e3, "gbs": unm_gbs, "hbm_frac": unm_gbs / hbm,
-                           "roofline_us": ub / (hbm * 1e9) * 1e6},
+                           "roofline_us": ub / (hbm * 1e9) * 1e6,
+                           "traffic": profiled_traffic("unmask", cfg.name)},
                 "step_roofline_us": step_roof_us, "step_frac": step_roof_us / (ms / a.steps * 1e3)},
             "gpu_launches": a.steps * launches_per_step(cfg),
             "graph": use_graph,
