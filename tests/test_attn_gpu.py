@@ -189,3 +189,13 @@ def test_device_errors_are_reported():
     long = synth.PagedCache(cache.k_pool, cache.v_pool, cache.page_table, np.array([64, 10 ** 6], np.int32),
                             cache.page_size, cache.dtype)
     assert _run(cfg, long, q, kb, vb, check_err=False)[2] == N.TT_ERR_BOUNDS
+
+
+def test_batch_above_one_launch_table():
+    """More sequences than one launch's sequence table holds (1024): the batch runs as several
+    launches; sequences on both sides of the cut and at the ends match the oracle."""
+    cfg = synth.CONFIGS["single"].replace(B=1100, Hq=16, Hkv=1, len_lo=0, len_hi=300,
+                                          qkv_scale=1.0)
+    cache, q, kb, vb = support.attention_case(cfg, seed=21)
+    pairs = [(b, 0) for b in (0, 1, 511, 1022, 1023, 1024, 1025, 1099)]
+    _check(cfg, cache, q, kb, vb, pairs=pairs)

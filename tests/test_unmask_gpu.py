@@ -123,3 +123,16 @@ def test_nothing_masked_and_empty_batch():
     api.tt_unmask(empty, torch.zeros((0, 16), dtype=torch.uint8, device="cuda"),
                   torch.zeros((0, 16), dtype=torch.int32, device="cuda"), 0.9, 1, 4)
     torch.cuda.synchronize()
+
+
+def test_large_batch_runs_the_chunked_kernel():
+    """B*S above the streaming kernel's row list (4096 rows) takes the chunked kernel; mixed
+    masked rows, every branch of the rules, bit-exact against the oracle."""
+    cfg = synth.CONFIGS["single"].replace(B=260, V=4096)
+    rng = np.random.default_rng(4)
+    lg = synth.draw_logits(cfg, seed=13, peak_hi=30.0)
+    masked = (rng.random((cfg.B, cfg.S)) < 0.7).astype(np.uint8)
+    masked[:8] = 0                                   # a few sequences with nothing masked
+    tokens = np.where(masked == 1, -1, 77).astype(np.int32)
+    for step in (1, 5, cfg.T):
+        _check_step(lg, "bf16", masked, tokens, cfg.tau, step, cfg.T)
