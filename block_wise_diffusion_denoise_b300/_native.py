@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtt_denoi
 TT_OK, TT_ERR_INVALID_ARG, TT_ERR_UNSUPPORTED, TT_ERR_CAPACITY, TT_ERR_CUDA, \
     TT_ERR_DEVICE_TIMEOUT, TT_ERR_BOUNDS = range(7)
 TT_BF16, TT_FP32 = 0, 1
-UNMASK_NOALLOC_SCRATCH_BYTES = 1024 * 1024   # TT_UNMASK_NOALLOC_SCRATCH_BYTES
+UNMASK_NOALLOC_SCRATCH_BYTES = 256 * 1024   # TT_UNMASK_NOALLOC_SCRATCH_BYTES
 
 STATUS_NAMES = {
     TT_OK: "TT_OK", TT_ERR_INVALID_ARG: "TT_ERR_INVALID_ARG", TT_ERR_UNSUPPORTED: "TT_ERR_UNSUPPORTED",

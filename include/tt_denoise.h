@@ -185,7 +185,7 @@ TT_API tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int
                     tt_stream_t stream);
 
 /* Largest scratch, in bytes, that tt_unmask_noalloc can use (its file-scope device array). */
-#define TT_UNMASK_NOALLOC_SCRATCH_BYTES (1024u * 1024u)
+#define TT_UNMASK_NOALLOC_SCRATCH_BYTES (256u * 1024u)
 
 /* tt_unmask for callers that cannot allocate device memory.  (The pages have no
  * counterpart of this call; it exists for deployment.)
