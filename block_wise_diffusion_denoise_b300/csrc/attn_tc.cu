@@ -13,36 +13,44 @@
 //    the MMAs.  Each CTA owns one 128-row M tile; when G*S = 256 two
 //    neighbouring CTAs of the persistent grid take the two halves of the same
 //    rows and walk the same pages at the same time, so the second read of every
-//    page is served by L2 and HBM sees each byte once.  One M tile per CTA
-//    leaves room in tensor memory for double-buffered 128-key S and P tiles.
+//    page is served by L2 and HBM sees each byte once.
+//  * Tensor memory (512 columns): O (128 fp32 columns), S (128, one tile, given
+//    back as soon as the softmax has read it), P (two buffers of 64 columns of
+//    packed bf16 pairs) and Q (64 columns of packed bf16 pairs).  Q lives in
+//    tensor memory as the A operand of the QK product, which frees its 32 KB of
+//    shared memory for a third V stage.
 //  * Tiles.  A key tile is two 64-token pages of the paged cache (or the block's
 //    own S keys).  Two producer warps move them with TMA (128-byte swizzle) into
-//    separate K and V rings (a K stage is free once QK has read it, a V stage
-//    once PV has), each fetching page ids 32 at a time; Q is loaded once per
-//    piece.
-//  * MMAs.  One warp issues S = Q K^T (M 128, N 128 keys) into a
-//    double-buffered TMEM tile, another issues O += P V (M 128, N 128 = D,
-//    K 128 keys) with P read from TMEM; one elected lane of a converged warp
-//    issues, so the descriptors stay warp-uniform.
+//    separate three-stage K and V rings (a K stage is free once QK has read it,
+//    a V stage once PV has), each fetching page ids 32 at a time; the K
+//    producer also starts each tile's V pages towards L2.  Q is written into
+//    tensor memory by the softmax warps once per piece.
+//  * MMAs.  One warp issues S = Q K^T (M 128, N 128 keys, A from tensor
+//    memory), another issues O += P V (M 128, N 128 = D, K 128 keys, A from
+//    tensor memory); one elected lane of a converged warp issues, so the
+//    descriptors stay warp-uniform.
 //  * Softmax.  Two warps share each TMEM lane quarter and take alternate tiles,
 //    one thread per row: the row's 128 scores come into registers at once and
-//    the S buffer goes back to the QK issuer immediately; the running maximum
-//    (log2 domain) is taken over from the partner's previous tile and only
-//    raised -- with a rescale of O in TMEM -- when the tile exceeds it by more
-//    than 2^8; P is written as packed bf16 into its own double-buffered TMEM
-//    tile.  The exponent phase of one tile overlaps the next QK product and the
-//    score phase of the partner's tile.  A register split (setmaxnreg) gives the
-//    softmax warpgroups 216 registers per thread and the role warps 64.  Columns past the valid keys of a partial tile
-//    are masked, and the matching V rows are zeroed before the PV product, so
-//    slots past L never matter.
+//    S goes back to the QK issuer immediately; the running maximum (log2
+//    domain) is taken over from the partner's previous tile and only raised --
+//    with a rescale of O in TMEM -- when the tile exceeds it by more than 2^8; P
+//    is written as packed bf16 into its own double-buffered TMEM tile.  The
+//    exponent phase of one tile overlaps the next QK product and the score
+//    phase of the partner's tile.  A register split (setmaxnreg) gives the
+//    softmax warpgroups 216 registers per thread and the role warps 64.
+//    Columns past the valid keys of a partial tile are masked, and the matching
+//    V rows are zeroed before the PV product, so slots past L never matter.
 //  * Work split.  The batch is a list of segments (b, g), each a run of
-//    two-page tiles plus one block tile (cost 8 and 1).  The persistent grid
-//    cuts the list into equal cost ranges, one per CTA group (stream-K style): a
-//    group that owns a whole segment writes the final output; pieces of a shared
-//    segment go to fp32 partial slots and the last CTA to finish the segment's
-//    M tile (atomic ticket, no waiting) merges them with log-sum-exp weights.
-//    Ragged and long contexts balance without host knowledge of the lengths,
-//    which live on the device.
+//    two-page tiles plus one block tile, counted in work units (a boundary
+//    charge per segment, then a tile, then the block tile).  When every group
+//    can take a whole segment and splitting would not pay, group i takes
+//    segment i; otherwise the persistent grid cuts the list into equal unit
+//    ranges, one per CTA group (stream-K style): a group that owns a whole
+//    segment writes the final output; pieces of a shared segment go to fp32
+//    partial slots and the last CTA to finish the segment's M tile (atomic
+//    ticket, no waiting) merges them with log-sum-exp weights.  Ragged and long
+//    contexts balance without host knowledge of the lengths, which live on the
+//    device.
 //  * Every mbarrier wait is bounded; a wait that gives up records
 //    TT_ERR_DEVICE_TIMEOUT, the CTA drains its copies and MMAs and exits.
 
@@ -65,7 +73,7 @@ constexpr int kD = 128;                  // head dim
 constexpr int kPage = 64;                // tokens per page
 constexpr int kTileKeys = 128;           // keys per context tile (two pages)
 constexpr int kKStages = 3;              // K ring depth (K is needed first: QK starts a tile)
-constexpr int kVStages = 2;              // V ring depth (V is needed last, after the softmax)
+constexpr int kVStages = 3;              // V ring depth (a V stage is held until PV completes)
 constexpr int kMaxCtas = 296;            // upper bound of the persistent grid (sizes the workspace)
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -84,8 +92,7 @@ constexpr int kCostSplit = 80;
 // stored as two 128-byte-swizzled halves of 64 columns (d 0..63 and d 64..127).
 constexpr int kHalf = 16384;             // 128 rows x 128 bytes
 constexpr int kStage = 2 * kHalf;        // one K or V tile (128 keys x 128 d)
-constexpr int kOffQ = 0;                 // Q[d-half]
-constexpr int kOffK = kStage;
+constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKStages * kStage;
 // Per-sequence table of one launch: clamped context lengths and the prefix sums of the
 // sequences' work units (at most kSeqMax sequences per launch; the host splits larger
@@ -98,10 +105,12 @@ constexpr int kSmemBytes = kOffSeqLen + 4 * kSeqMax + 1024;
 // TMEM columns (one M tile per CTA).
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;                 // O: 128 fp32 columns
-constexpr int kColS = 128;               // S[buf]: 128 fp32 columns each
-constexpr int kColP = 384;               // P[buf]: 64 columns of packed bf16 pairs each
+constexpr int kColS = 128;               // S: 128 fp32 columns (released as soon as it is read)
+constexpr int kColP = 256;               // P[buf]: 64 columns of packed bf16 pairs each
+constexpr int kColQ = 384;               // Q: 64 columns of packed bf16 pairs (the A operand of QK)
 
 struct TcParams {
+    const uint16_t *q;            // [B, S, Hq, D] block queries (read into TMEM per piece)
     const int32_t *page_table;
     const int32_t *ctx_len;
     int num_pages, max_pages;
@@ -121,8 +130,10 @@ struct Bars {
     uint64_t q_full, q_empty;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2];    // S of the tile is in TMEM (QK committed)
-    uint64_t s_empty[2];   // the tile's four softmax warps have read S
+    uint64_t s_full[2];    // [tile parity] S of the tile is in TMEM (QK committed).  One barrier
+                           // per parity, so each is waited by one warp set in phase order (a
+                           // shared one could be passed a phase early by the other set).
+    uint64_t s_empty;      // the tile's four softmax warps have read S (waited by QK only)
     uint64_t p_full[2];    // the tile's four softmax warps wrote P
     uint64_t p_free[2];    // the PV product that read P has completed
     uint64_t pub[2][4];    // [tile parity][lane quarter]: the running maximum after the tile is published
@@ -350,13 +361,13 @@ __device__ __forceinline__ float softmax_chunk(const uint32_t (&sv)[32], uint64_
 
 // ------------------------------------------------------------------ the kernel
 //
-// Warps: 0 TMA producer of Q and K; 1 QK issuer; 2 PV issuer; 3 TMA producer of V;
+// Warps: 0 TMA producer of K; 1 QK issuer; 2 PV issuer; 3 TMA producer of V;
 // 4..11 softmax and epilogue
 // (two warps per TMEM lane quarter taking alternate tiles; at the end of a piece each
 // writes half of the O columns).
 
 __global__ void __launch_bounds__(384, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
                const __grid_constant__ CUtensorMap tm_vb, const TcParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -368,24 +379,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     Bars &bar = sh.bar;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar.q_full, 1);
+        mbar_init(&bar.q_full, 4);
         mbar_init(&bar.q_empty, 1);
         for (int s = 0; s < kKStages; ++s) { mbar_init(&bar.k_full[s], 1); mbar_init(&bar.k_empty[s], 1); }
         for (int s = 0; s < kVStages; ++s) { mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1); }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&bar.s_full[s], 1);
-            mbar_init(&bar.s_empty[s], 4);
+
             mbar_init(&bar.p_full[s], 4);
             mbar_init(&bar.p_free[s], 1);
             for (int q = 0; q < 4; ++q) mbar_init(&bar.pub[s][q], 1);
         }
+        mbar_init(&bar.s_full[0], 1);
+        mbar_init(&bar.s_full[1], 1);
+        mbar_init(&bar.s_empty, 4);
         mbar_init(&bar.o_full, 1);
         mbar_init(&bar.o_empty, 8);
         mbar_init(&bar.grp, 8);
         for (int i = 0; i < 2; ++i) mbar_init(&bar.done[i], 1);
         fence_mbar_init();
         sh.abort = 0;
-        prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_kb); prefetch_tmap(&tm_vb);
     }
     // the sequence table: lengths loaded by all threads at once, prefix sums by warp 2
@@ -432,7 +445,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == 0 || warp == 3) {
         regs_release();
         // ================================================================ TMA producers
-        // Warp 0 loads Q and K, warp 3 loads V, so that a K copy never waits behind the
+        // Warp 0 loads K, warp 3 loads V, so that a K copy never waits behind the
         // release of a V stage (they are freed by different products).  Each whole warp
         // walks the work (page ids are fetched 32 at a time, one per lane); lane 0 issues
         // the copies.
@@ -445,18 +458,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         unsigned char *ring = sm + (is_v ? kOffV : kOffK);
         Piece pc;
         int qi = 0, t = 0;
-        bool issued = false;
         while (it.next(p, pc)) {
-            if (!is_v) {
-                if (!wait_bar(sh, &bar.q_empty, (qi & 1) ^ 1, p.dev_err)) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bar.q_full, (uint32_t)kStage);
-                    for (int dh = 0; dh < 2; ++dh)
-                        tma_load_3d(sm + kOffQ + dh * kHalf, &tm_q, &bar.q_full, 64 * dh, pc.g * G,
-                                    pc.b * S + mt * (128 / G));
-                }
-                issued = true;
-            }
             bool ok = true;
             int my_page = 0;
             for (int i = pc.first; i < pc.last; ++i, ++t) {
@@ -502,7 +504,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         // Drain: every copy issued must land before the CTA may exit.  The last copy into
         // a stage completes that stage's latest phase.
-        if (issued) mbar_wait(&bar.q_full, (uint32_t)(qi - 1) & 1, kWaitLimit);
         for (int k = 1; k <= nst && t - k >= 0; ++k)
             mbar_wait(&full[(t - k) % nst], (uint32_t)((t - k) / nst) & 1, kWaitLimit);
         __syncwarp();
@@ -512,30 +513,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         Piece pc;
         int qi = 0, t = 0;
         bool ok = true;
-        const uint32_t qa = smem_u32(sm + kOffQ);
         while (ok && it.next(p, pc)) {
             if (!wait_bar(sh, &bar.q_full, qi & 1, p.dev_err)) break;
             tc_fence_after();
             const int ntiles = pc.last - pc.first;
             for (int j = 0; j < ntiles; ++j, ++t) {
-                const int kst = t % kKStages, sb = t & 1;
+                const int kst = t % kKStages;
                 const int valid = tile_valid(pc, pc.first + j, S);
                 const int nk = (valid + 15) & ~15;
                 if (!wait_bar(sh, &bar.k_full[kst], (uint32_t)(t / kKStages) & 1, p.dev_err)) { ok = false; break; }
-                if (!wait_bar(sh, &bar.s_empty[sb], (((uint32_t)t >> 1) & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                // S is single-buffered: the previous tile's scores must have been read
+                if (t > 0 && !wait_bar(sh, &bar.s_empty, (uint32_t)(t - 1) & 1, p.dev_err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, nk, false, false);
                 const uint32_t kb = smem_u32(sm + kOffK + kst * kStage);
-                const uint32_t dcol = tmem + kColS + 128 * sb;
+                const uint32_t dcol = tmem + kColS;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t da = sdesc_sw128(qa + (kk >> 2) * (uint32_t)kHalf + (kk & 3) * 32, 16, 1024);
+                for (int kk = 0; kk < 8; ++kk) {   // 16 head dimensions per step; Q from TMEM
                     const uint64_t db = sdesc_sw128(kb + (kk >> 2) * (uint32_t)kHalf + (kk & 3) * 32, 16, 1024);
-                    if (elect_one()) mma_bf16_ss(dcol, da, db, idesc, kk > 0);
+                    if (elect_one()) mma_bf16_ts(dcol, tmem + kColQ + 8 * kk, db, idesc, kk > 0);
                     __syncwarp();
                 }
                 if (elect_one()) {
-                    mma_commit(&bar.s_full[sb]);
+                    mma_commit(&bar.s_full[t & 1]);
                     mma_commit(&bar.k_empty[kst]);
                     if (j == ntiles - 1) mma_commit(&bar.q_empty);
                 }
@@ -614,20 +614,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int s_pos = r / G, hh = r % G;
         const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
         const float c2 = p.scale_log2;
-        Piece pc;
+        // Q of a piece into TMEM (the A operand of QK): the h = 0 warps write their rows,
+        // once the QK products of the previous piece are done with the old Q.
+        int qn = 0;
+        auto load_q = [&](const Piece &qc) -> bool {
+            if (qn > 0 && !wait_bar(sh, &bar.q_empty, (uint32_t)(qn - 1) & 1, p.dev_err)) return false;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + (((size_t)qc.b * S + s_pos) * p.Hq + qc.g * G + hh) * kD);
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t w[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 v = __ldg(src + 8 * half + k);
+                    w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+                }
+                tmem_st32(tmem + lane_off + kColQ + 32 * half, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.q_full);
+            ++qn;
+            return true;
+        };
+        Piece pc, npc;
         int t = 0, pi = 0, k_grp = 0;
         bool ok = true;
-        while (ok && it.next(p, pc)) {
+        bool have = it.next(p, pc);
+        if (have && h == 0) ok = load_q(pc);
+        while (ok && have) {
             float m_l = -INFINITY, l = 0.f;              // my row sum and the maximum it is scaled by
             float m_last = -INFINITY;                    // maximum after my latest tile
             const int ntiles = pc.last - pc.first;
             for (int j = 0; j < ntiles; ++j, ++t) {
                 if ((t & 1) != h) continue;              // the partner's tile
-                const int sb = h;
+                const int sb = h;                        // P buffer of this tile
                 const int valid = tile_valid(pc, pc.first + j, S);
-                if (!wait_bar(sh, &bar.s_full[sb], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
+                if (!wait_bar(sh, &bar.s_full[h], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t scol = tmem + lane_off + kColS + 128 * sb;
+                const uint32_t scol = tmem + lane_off + kColS;
                 // ---- the row's 128 scores into registers (all loads in flight at once), its
                 // maximum, and S released to the next QK product right away
                 uint32_t a0[32], a1[32], a2[32], a3[32];
@@ -638,7 +665,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
+                if (lane == 0) mbar_arrive(&bar.s_empty);
                 if (valid < kTileKeys) {   // warp-uniform
                     mask_scores(a0, 0, valid);
                     mask_scores(a1, 32, valid);
@@ -710,6 +737,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (lane == 0) mbar_arrive(&bar.p_full[sb]);
             }
             if (!ok) break;
+            // the next piece's Q, ahead of this piece's epilogue so that its QK can start
+            const bool have_next = it.next(p, npc);
+            if (have_next && h == 0 && !load_q(npc)) { ok = false; break; }
             // ---------------------------------------------------------- epilogue of the piece
             if (!wait_bar(sh, &bar.o_full, pi & 1, p.dev_err)) { ok = false; break; }
             tc_fence_after();
@@ -831,6 +861,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
             ++pi;
+            pc = npc;
+            have = have_next;
         }
     }
 
@@ -907,13 +939,7 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     const int G = a.Hq / a.Hkv;
     const int rows = G * a.S;
     const int cps = rows / 128;   // CTAs per segment, one per 128-row M tile
-    CUtensorMap mq, mk, mv, mkb, mvb;
-    {
-        const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)nb * a.S};
-        const uint64_t str[2] = {(uint64_t)kD * 2, (uint64_t)a.Hq * kD * 2};
-        const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(128 / G)};
-        if (!make_map(&mq, q, 3, dims, str, box)) return TT_ERR_CUDA;
-    }
+    CUtensorMap mk, mv, mkb, mvb;
     {
         const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)kPage, (uint64_t)a.Hkv, (uint64_t)c.num_pages};
         const uint64_t str[3] = {(uint64_t)kD * 2, (uint64_t)kPage * kD * 2, (uint64_t)a.Hkv * kPage * kD * 2};
@@ -929,6 +955,7 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
         if (!make_map(&mvb, v_blk, 3, dims, str, box)) return TT_ERR_CUDA;
     }
     TcParams p;
+    p.q = q;
     p.page_table = c.page_table + (size_t)b0 * c.max_pages_per_seq;
     p.ctx_len = c.ctx_len + b0;
     p.num_pages = c.num_pages;
@@ -949,7 +976,7 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
         return TT_ERR_CUDA;
-    attn_tc_kernel<<<n_groups * cps, 384, kSmemBytes, a.stream>>>(mq, mk, mv, mkb, mvb, p);
+    attn_tc_kernel<<<n_groups * cps, 384, kSmemBytes, a.stream>>>(mk, mv, mkb, mvb, p);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
