@@ -25,7 +25,7 @@ STATUS_NAMES = {
 # Every symbol the header declares, in declaration order.
 EXPORTED = ("tt_status_string", "tt_version", "tt_denoise_attn_workspace_size", "tt_denoise_attn",
             "tt_unmask_workspace_size", "tt_unmask", "tt_unmask_noalloc", "tt_kv_append",
-            "tt_block_step_workspace_size", "tt_block_step", "tt_get_device_error")
+            "tt_block_step_workspace_size", "tt_block_step", "tt_get_device_error", "tt_check_wait_timeout")
 
 
 class NativeLibraryMissing(ImportError):
@@ -77,6 +77,7 @@ _SIGNATURES = {
     "tt_block_step": (_I, [ctypes.POINTER(tt_kv_cache), _I, _PP, _PP, _PP, _PP, _P, _I, _I, _I, _I, _F, _I,
                            _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tt_get_device_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "tt_check_wait_timeout": (_I, [ctypes.c_uint32, _P, _P]),
 }
 
 _lib = None

@@ -271,3 +271,11 @@ def tt_get_device_error(dev_err: torch.Tensor, stream: Optional[torch.cuda.Strea
     N.check(N.lib().tt_get_device_error(dev_err.data_ptr(), _stream(stream), ctypes.byref(code)),
             "tt_get_device_error")
     return int(code.value)
+
+
+def tt_check_wait_timeout(polls: int, dev_err: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch the library's bounded-wait self-check: a wait that can never finish gives up
+    after `polls` polls and records TT_ERR_DEVICE_TIMEOUT in `dev_err` (read it with
+    tt_get_device_error)."""
+    _need(dev_err, "dev_err", dtype=torch.int32)
+    N.check(N.lib().tt_check_wait_timeout(int(polls), dev_err.data_ptr(), _stream(stream)), "tt_check_wait_timeout")

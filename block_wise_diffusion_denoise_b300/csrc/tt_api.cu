@@ -207,6 +207,11 @@ tt_status tt_block_step(const tt_kv_cache *ctx, int n_layers, const void *const 
                      committed_now, conf, n_masked, uws, ws_bytes - attn_region, dev_err, stream);
 }
 
+tt_status tt_check_wait_timeout(uint32_t polls, uint32_t *dev_err, tt_stream_t stream) {
+    if (dev_err == nullptr || polls < 1 || polls > (1u << 24)) return TT_ERR_INVALID_ARG;
+    return tt::launch_wait_check(polls, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 tt_status tt_get_device_error(const uint32_t *dev_err, tt_stream_t stream, uint32_t *host_code) {
     if (dev_err == nullptr || host_code == nullptr) return TT_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -256,6 +256,16 @@ TT_API tt_status tt_block_step(const tt_kv_cache *ctx, int n_layers, const void 
  * finished (synchronises the stream).  The word is not cleared. */
 TT_API tt_status tt_get_device_error(const uint32_t *dev_err, tt_stream_t stream, uint32_t *host_code);
 
+/* Self-check of the failure path every kernel uses (the pages have no counterpart;
+ * it exists so that a caller can see, without faulting or hanging a GPU, that a
+ * wait that can never finish gives up and reports).  Launches one warp that waits
+ * on a shared-memory mbarrier which nothing arrives at, polling it at most
+ * `polls` times (1 <= polls <= 2^24) with the same bounded wait the kernels use,
+ * then records TT_ERR_DEVICE_TIMEOUT in dev_err (device word, required) and
+ * exits; the context stays usable.  Returns TT_ERR_INVALID_ARG for a bad
+ * argument, TT_ERR_CUDA if the launch fails. */
+TT_API tt_status tt_check_wait_timeout(uint32_t polls, uint32_t *dev_err, tt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

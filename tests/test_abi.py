@@ -140,3 +140,10 @@ def test_block_step_and_error_word_reject_bad_arguments(lib):
     code = ctypes.c_uint32(0)
     assert lib.tt_get_device_error(None, None, ctypes.byref(code)) == N.TT_ERR_INVALID_ARG
     assert lib.tt_get_device_error(0x1000, None, None) == N.TT_ERR_INVALID_ARG
+
+
+def test_wait_self_check_rejects_bad_arguments_on_the_host(lib):
+    fake = ctypes.c_void_p(0x10000)          # never dereferenced: validation fails first
+    assert lib.tt_check_wait_timeout(0, fake, None) == N.TT_ERR_INVALID_ARG
+    assert lib.tt_check_wait_timeout((1 << 24) + 1, fake, None) == N.TT_ERR_INVALID_ARG
+    assert lib.tt_check_wait_timeout(100, None, None) == N.TT_ERR_INVALID_ARG
