@@ -288,6 +288,24 @@ def config_dict(cfg, a):
             "l2": "inputs larger than L2, two copies alternate between steps"}
 
 
+# --------------------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of its own batch in at most max_ms."""
+    return world * steps / (max_ms / 1e3)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def run_ours(a, cfg):
@@ -429,10 +447,7 @@ def run_ours(a, cfg):
             ev1.synchronize()
     barrier()
     ms = ev0.elapsed_time(ev1)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = max_over_ranks(ms, world, dev)
     code = api.tt_get_device_error(err)
     if code != 0:
         raise SystemExit(f"device error {code} during the timed region")
@@ -485,10 +500,8 @@ def run_ours(a, cfg):
         e1.record()
         e1.synchronize()
         e_ms = e0.elapsed_time(e1) / a.e2e_steps
-        et = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e = {"value": world / (float(et.item()) / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": job_rate(world, 1, e_ms), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": a.e2e_steps}
 
     if rank == 0:
@@ -504,7 +517,7 @@ def run_ours(a, cfg):
         attn_tfs = af / (attn_ms * 1e-3) / 1e12
         unm_gbs = ub / (unmask_ms * 1e-3) / 1e9
         step_roof_us = max(ab / (hbm * 1e9), af / (tc * 1e12)) * 1e6 + ub / (hbm * 1e9) * 1e6
-        value = world * a.steps / (ms / 1e3)
+        value = job_rate(world, a.steps, ms)
         line = {
             "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms / a.steps, "higher_is_better": True, "scaling": "weak",
