@@ -451,6 +451,8 @@ __device__ void stream_rules(const StreamParams &p, const int *rows, int R, int 
         float m = -INFINITY, z = 0.f;
         int a = INT_MAX;
         for (int w = w0; w <= w1; ++w) {
+            // a warp whose share is empty (fewer units than warps) wrote no partial
+            if ((long long)(w + 1) * NU / NW == (long long)w * NU / NW) continue;
             const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part + w + k));
             merge(m, z, a, v.x, v.y, __float_as_int(v.z));
         }
