@@ -10,10 +10,10 @@
 // Design for sm_103a:
 //  * Rows.  The G = Hq/Hkv query heads of one KV head share every key, so the
 //    G*S (s, head) rows of one (sequence, KV head) segment form the M side of
-//    the MMAs.  Each CTA owns one 128-row M tile; when G*S = 256 two
-//    neighbouring CTAs of the persistent grid take the two halves of the same
-//    rows and walk the same pages at the same time, so the second read of every
-//    page is served by L2 and HBM sees each byte once.
+//    the MMAs.  Each CTA owns one 128-row M tile; when G*S is a larger
+//    multiple of 128, neighbouring CTAs of the persistent grid (a group) take
+//    the M tiles of the same rows and walk the same pages at the same time, so
+//    the later reads of every page are served by L2 and HBM sees each byte once.
 //  * Tensor memory (512 columns): O (128 fp32 columns), S (128, one tile, given
 //    back as soon as the softmax has read it), P (two buffers of 64 columns of
 //    packed bf16 pairs) and Q (64 columns of packed bf16 pairs).  Q lives in
@@ -916,14 +916,15 @@ bool attn_tc_supported(int S, int Hq, int Hkv, int D, int page_size, tt_dtype dt
     if (dtype != TT_BF16 || D != kD || page_size != kPage || Hkv < 1 || Hq % Hkv != 0) return false;
     const int G = Hq / Hkv;
     const int rows = G * S;
-    return (S % 16 == 0) && S <= kTileKeys && (rows == 128 || rows == 256) && (128 % G == 0);
+    // whole 128-row M tiles, one CTA each, at most 16 CTAs per segment
+    return (S % 16 == 0) && S <= kTileKeys && rows % 128 == 0 && rows <= 16 * 128;
 }
 
 size_t attn_tc_ws_bytes(int B, int S, int Hq, int Hkv, int D) {
     const size_t rows = (size_t)rows_of(S, Hq, Hkv);
     const size_t slot = (rows * D + 2 * rows) * sizeof(float);
     const size_t nseg = (size_t)(B < kSeqMax ? B : kSeqMax) * Hkv;   // one launch's segments
-    return align_up(2 * nseg * sizeof(unsigned), 256) + (kMaxCtas + nseg) * slot;
+    return align_up(rows / 128 * nseg * sizeof(unsigned), 256) + (kMaxCtas + nseg) * slot;
 }
 
 namespace {
@@ -970,7 +971,7 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     p.n_groups = n_groups;
     const size_t nseg = (size_t)nb * a.Hkv;
     p.tickets = static_cast<unsigned *>(a.ws);
-    p.part = reinterpret_cast<float *>(static_cast<char *>(a.ws) + align_up(2 * nseg * sizeof(unsigned), 256));
+    p.part = reinterpret_cast<float *>(static_cast<char *>(a.ws) + align_up((size_t)cps * nseg * sizeof(unsigned), 256));
     p.slot_floats = (long long)rows * kD + 2LL * rows;
     p.dev_err = a.dev_err;
     if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=

@@ -199,3 +199,13 @@ def test_batch_above_one_launch_table():
     cache, q, kb, vb = support.attention_case(cfg, seed=21)
     pairs = [(b, 0) for b in (0, 1, 511, 1022, 1023, 1024, 1025, 1099)]
     _check(cfg, cache, q, kb, vb, pairs=pairs)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv", [(32, 32, 2), (64, 16, 2), (48, 16, 2), (128, 4, 2), (16, 24, 1)])
+def test_tensor_core_shapes_beyond_two_m_tiles(S, Hq, Hkv):
+    """Block sizes and head groupings with 3 to 16 M tiles of 128 rows per segment (S = 32, 48,
+    64, 128; 24 query heads per KV head) on the tensor-core kernel, ragged contexts, stress
+    values, against the oracle."""
+    cfg = synth.CONFIGS["single"].replace(B=3, S=S, Hq=Hq, Hkv=Hkv, qkv_scale=1.0)
+    cache, q, kb, vb = support.attention_case(cfg, seed=S + Hq, lens=[0, 700, 1500])
+    _check(cfg, cache, q, kb, vb)
