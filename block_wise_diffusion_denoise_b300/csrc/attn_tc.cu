@@ -457,7 +457,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         uint64_t *empty = is_v ? bar.v_empty : bar.k_empty;
         unsigned char *ring = sm + (is_v ? kOffV : kOffK);
         Piece pc;
-        int qi = 0, t = 0;
+        int t = 0;
         while (it.next(p, pc)) {
             bool ok = true;
             int my_page = 0;
@@ -499,7 +499,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                 }
             }
-            ++qi;
             if (!ok) break;
         }
         // Drain: every copy issued must land before the CTA may exit.  The last copy into
