@@ -444,7 +444,7 @@ __device__ void stream_rules(const StreamParams &p, const int *rows, int R, int 
     // per masked row: merge its partials (group order) into (conf, argmax)
     int n_commit = 0;
     float best_conf = -1.f;
-    int best_pos = INT_MAX;
+    int best_pos = INT_MAX, best_arg = 0;
     for (int k = k0 + lane; k < k1; k += 32) {
         const int w0 = unit_owner((long long)k * p.nc, NU, NW);
         const int w1 = unit_owner((long long)(k + 1) * p.nc - 1, NU, NW);
@@ -462,36 +462,27 @@ __device__ void stream_rules(const StreamParams &p, const int *rows, int R, int 
         if (p.conf) p.conf[rr] = cf;
         const bool c = last_step || cf >= p.tau;
         n_commit += c ? 1 : 0;
-        if (cf > best_conf || (cf == best_conf && pos < best_pos)) { best_conf = cf; best_pos = pos; }
+        if (cf > best_conf || (cf == best_conf && pos < best_pos)) { best_conf = cf; best_pos = pos; best_arg = a; }
         if (c) { p.tokens[rr] = a; p.masked[rr] = 0; }
         if (p.committed_now) p.committed_now[rr] = c ? 1 : 0;
-        if (!c) {
-            // keep the argmax for a possible fallback commit, in the (consumed) partial
-            // slot of the row's first warp
-            UnmaskPartial q;
-            q.m = cf; q.z = 0.f; q.arg = a; q.pad = pos;
-            p.part[w0 + k] = q;
-        }
     }
     // warp totals: commits and the most confident masked position (lowest position on ties)
     for (int o = 16; o > 0; o >>= 1) {
         n_commit += __shfl_xor_sync(0xffffffffu, n_commit, o);
         const float oc = __shfl_xor_sync(0xffffffffu, best_conf, o);
         const int op = __shfl_xor_sync(0xffffffffu, best_pos, o);
-        if (oc > best_conf || (oc == best_conf && op < best_pos)) { best_conf = oc; best_pos = op; }
+        const int oa = __shfl_xor_sync(0xffffffffu, best_arg, o);
+        if (oc > best_conf || (oc == best_conf && op < best_pos)) { best_conf = oc; best_pos = op; best_arg = oa; }
     }
     const int n_m = k1 - k0;
     int fallback = 0;
-    __syncwarp();   // the stashed (conf, argmax) entries are visible to lane 0
     if (n_commit == 0 && n_m > 0) {
         // nothing reached the threshold: commit the single most confident masked position
+        // (its argmax travelled with it through the reduction)
         fallback = 1;
-        const int k = lower_bound_rows(rows + k0, n_m, b * p.S + best_pos) + k0;
         if (lane == 0) {
-            const int w0 = unit_owner((long long)k * p.nc, NU, NW);
-            const UnmaskPartial q = p.part[w0 + k];
-            const size_t rr = (size_t)rows[k];
-            p.tokens[rr] = q.arg;
+            const size_t rr = (size_t)b * p.S + best_pos;
+            p.tokens[rr] = best_arg;
             p.masked[rr] = 0;
             if (p.committed_now) p.committed_now[rr] = 1;
         }
