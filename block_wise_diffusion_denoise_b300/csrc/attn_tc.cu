@@ -87,6 +87,8 @@ constexpr int kCostTile = 8, kCostBlock = 6, kCostSeg = 24;
 // a whole segment and the longest one is within this margin of the even split, each
 // group takes one whole segment instead.
 constexpr int kCostSplit = 80;
+// A stream-K group gets at least this many units (eight tiles) of work.
+constexpr int kMinGroupUnits = 64;
 
 // Shared memory (offsets from a 1024-byte aligned base).  Every 128-row operand is
 // stored as two 128-byte-swizzled halves of 64 columns (d 0..63 and d 64..127).
@@ -171,6 +173,7 @@ struct Piece {
 // starts at unit X starts at unit X + kCostSeg + kCostTile * i (the block tile is i = ntc).
 struct WorkIter {
     long long U, lo, hi, X;
+    int NG;                 // groups that share the work (the stream-K split's divisor)
     int b, g, L, ntc, C;
     int B, Hkv;
     const long long *pre;   // shared: prefix sums of the sequences' work units
@@ -181,6 +184,7 @@ struct WorkIter {
         U = pre[B];
         const long long nseg = (long long)B * Hkv;
         const long long max_seg = seq_cost(max_len, 1);
+        NG = p.n_groups;
         if (nseg <= p.n_groups && max_seg <= U / p.n_groups + kCostSplit) {
             // one whole segment per group: the range of segment `group` exactly
             if (group < nseg) {
@@ -191,8 +195,16 @@ struct WorkIter {
                 lo = hi = U;
             }
         } else {
-            lo = (long long)group * U / p.n_groups;
-            hi = (long long)(group + 1) * U / p.n_groups;
+            // stream-K over at most U / kMinGroupUnits groups, so that a small batch is not
+            // cut into one-tile pieces whose merges would cost more than the tiles
+            const long long ng = U / kMinGroupUnits;
+            NG = (int)(ng < 1 ? 1 : (ng < p.n_groups ? ng : p.n_groups));
+            if (group < NG) {
+                lo = (long long)group * U / NG;
+                hi = (long long)(group + 1) * U / NG;
+            } else {
+                lo = hi = U;
+            }
         }
         // the first sequence that ends after lo
         int a = 0, z = B;
@@ -815,7 +827,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     // rescale, so each piece costs one round trip (its maximum, sum and 64
                     // output values are loaded together).
                     const long long U = it.U;
-                    const int n = p.n_groups;
+                    const int n = it.NG;
                     const int c_first = owner(pc.X + kCostSeg, U, n);
                     const int c_last = owner(pc.X + kCostSeg + (long long)kCostTile * pc.ntc, U, n);
                     float M = -INFINITY, Lsum = 0.f;

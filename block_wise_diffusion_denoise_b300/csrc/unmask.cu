@@ -344,6 +344,7 @@ constexpr int kSStages = 2;
 constexpr int kSChunkBytes = 6144;
 constexpr int kSRowsMax = 4096;           // masked-row list held in shared memory
 constexpr int kSCtasMax = 296;            // grid cap (sizes the workspace)
+constexpr int kSMinUnits = 4;             // a warp's share is at least this many units
 constexpr int kSSmemBytes = kSWarps * kSStages * kSChunkBytes;
 
 struct StreamParams {
@@ -546,9 +547,13 @@ __global__ void __launch_bounds__(kSThreads, 1) unmask_stream_kernel(const Strea
         if (lane == 0 && p.n_masked) p.n_masked[b] = 0;
     }
 
-    // ---- this warp's units
-    const int NW = gridDim.x * kSWarps, w = blockIdx.x * kSWarps + warp;
+    // ---- this warp's units: the shares go to at most NU / kSMinUnits warps, so that a
+    // small batch is not spread over warps of one unit each (every share is a partial
+    // the rule stage must read)
     const long long NU = (long long)R * p.nc;
+    const int NWall = gridDim.x * kSWarps, w = blockIdx.x * kSWarps + warp;
+    const int NW = (int)(NU / kSMinUnits < 1 ? 1 : (NU / kSMinUnits < NWall ? NU / kSMinUnits : NWall));
+    if (w >= NW) return;
     const long long u0 = (long long)w * NU / NW, u1 = (long long)(w + 1) * NU / NW;
     const int n = (int)(u1 - u0);
     if (n <= 0) return;
