@@ -34,7 +34,9 @@ Readings where the pages are silent (each is listed with its reason in the
 repository's design notes): the softmax scale is an argument (default
 1/sqrt(D)); GQA head h reads KV head floor(h / G); every context position
 precedes the block, so "causal" towards the context admits all L keys; no
-mask inside the block; no positional logic (q and k arrive position-encoded);
+mask inside the block for the denoiser, while the context tower, taking in a
+committed block, lets block position i see block positions 0..i (its causal
+order applied within the block); no positional logic (q and k arrive position-encoded);
 confidence is the maximum softmax probability at temperature 1; a position is
 committed when conf >= tau; if none qualifies the single most confident
 masked position is committed (lowest position on ties); at step T every
@@ -83,7 +85,8 @@ def context_rows(pool: np.ndarray, page_table_row: np.ndarray, L: int, page_size
 
 def denoise_attention_seq(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
                           k_blk: np.ndarray, v_blk: np.ndarray, sm_scale: float,
-                          key_bias: Optional[np.ndarray] = None, return_probs: bool = False):
+                          key_bias: Optional[np.ndarray] = None, return_probs: bool = False,
+                          causal_block: bool = False):
     """Two-segment attention of one sequence's block queries ([A], [G], [R]).
 
     q [S, Hq, D]; k_ctx, v_ctx [L, Hkv, D] (context tower KV of this layer, L may
@@ -95,6 +98,12 @@ def denoise_attention_seq(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
         p   = softmax(s)                        (over all L + S keys)
         o_{i,h} = sum_j p_j v_{j,g}
 
+    With ``causal_block`` the block is read the way the frozen context tower
+    reads it when it takes in a committed block ([A]: that tower is a causal
+    autoregressive model over the prompt and the committed tokens; [G]: after a
+    commit it extends its state with the clean block): block query i still sees
+    every context key, but of the block keys only j <= i.
+
     ``key_bias`` (optional, [L + S]) is added to every score of the key; -inf
     removes a key.  Returns o [S, Hq, D] and lse [Hq, S] = log sum_j exp(s_j)
     (natural log); with ``return_probs`` also p [Hq, S, L + S].
@@ -102,8 +111,14 @@ def denoise_attention_seq(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
     S, Hq, D = q.shape
     Hkv = k_blk.shape[1]
     G = Hq // Hkv
+    L = k_ctx.shape[0]
     K = np.concatenate([k_ctx, k_blk], axis=0)      # [L+S, Hkv, D]
     Vv = np.concatenate([v_ctx, v_blk], axis=0)
+    # visible[i, j]: may block query i read key j of [context ; block]?
+    visible = np.ones((S, L + S), dtype=bool)
+    if causal_block:
+        for i in range(S):
+            visible[i, L + i + 1:] = False
     o = np.empty((S, Hq, D), dtype=np.float64)
     lse = np.empty((Hq, S), dtype=np.float64)
     probs = np.empty((Hq, S, K.shape[0]), dtype=np.float64) if return_probs else None
@@ -112,6 +127,7 @@ def denoise_attention_seq(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
         s = sm_scale * (q[:, h, :] @ K[:, g, :].T)   # [S, L+S]
         if key_bias is not None:
             s = s + key_bias[None, :]
+        s = np.where(visible, s, -np.inf)
         m = s.max(axis=1, keepdims=True)
         e = np.exp(s - m)
         z = e.sum(axis=1, keepdims=True)
@@ -128,12 +144,13 @@ def denoise_attention_seq(q: np.ndarray, k_ctx: np.ndarray, v_ctx: np.ndarray,
 def denoise_attention(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray,
                       ctx_len: np.ndarray, page_size: int, q: np.ndarray, k_blk: np.ndarray,
                       v_blk: np.ndarray, sm_scale: float, dtype: str,
-                      seqs: Optional[Sequence[int]] = None):
+                      seqs: Optional[Sequence[int]] = None, causal_block: bool = False):
     """Batched two-segment attention over a paged context cache.
 
     Shapes as stored: pools [num_pages, Hkv, page_size, D]; page_table [B, max_pages];
     q [B, S, Hq, D]; k_blk, v_blk [B, S, Hkv, D].  ``seqs`` restricts the work to some
-    sequences (the others are returned as NaN).  Returns o [B, S, Hq, D] and lse [B, Hq, S].
+    sequences (the others are returned as NaN).  ``causal_block`` as in
+    ``denoise_attention_seq``.  Returns o [B, S, Hq, D] and lse [B, Hq, S].
     """
     B, S, Hq, D = q.shape
     o = np.full((B, S, Hq, D), np.nan)
@@ -143,7 +160,8 @@ def denoise_attention(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.nda
         kc = decode(context_rows(k_pool, page_table[b], L, page_size), dtype)
         vc = decode(context_rows(v_pool, page_table[b], L, page_size), dtype)
         o[b], lse[b] = denoise_attention_seq(decode(q[b], dtype), kc, vc, decode(k_blk[b], dtype),
-                                             decode(v_blk[b], dtype), sm_scale)
+                                             decode(v_blk[b], dtype), sm_scale,
+                                             causal_block=causal_block)
     return o, lse
 
 

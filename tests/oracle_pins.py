@@ -53,9 +53,10 @@ def _sdpa(q, K, V, scale, G):
     return o[0].numpy().transpose(1, 0, 2)                                      # [S, Hq, D]
 
 
-def _brute_attention(q, pool_k, pool_v, table, L, page_size, kb, vb, scale):
+def _brute_attention(q, pool_k, pool_v, table, L, page_size, kb, vb, scale, causal_block=False):
     """Pure-Python attention: enumerate the visible keys by scanning the pages, weight each
     value by exp(score) and divide by the total weight (inputs are small, no overflow).
+    With ``causal_block`` block query i skips the block keys after position i.
     Returns the outputs [S, Hq, D] and log(total weight) [Hq, S]."""
     S, Hq, D = q.shape
     Hkv = kb.shape[1]
@@ -71,21 +72,23 @@ def _brute_attention(q, pool_k, pool_v, table, L, page_size, kb, vb, scale):
             pos = owner[page] * page_size + slot
             if pos < L:
                 keys.append((pool_k[page, :, slot, :], pool_v[page, :, slot, :]))
-    for s in range(S):
-        keys_blk = (kb[s], vb[s])
-        keys.append(keys_blk)
     out = np.zeros((S, Hq, D))
     lse = np.zeros((Hq, S))
     for i in range(S):
+        seen = list(keys)
+        for s in range(S):
+            if causal_block and s > i:
+                break
+            seen.append((kb[s], vb[s]))
         for h in range(Hq):
             g = h // G
             w = []
-            for kr, _ in keys:
+            for kr, _ in seen:
                 w.append(math.exp(scale * math.fsum(float(q[i, h, d]) * float(kr[g, d]) for d in range(D))))
             tot = math.fsum(w)
             lse[h, i] = math.log(tot)
             for d in range(D):
-                out[i, h, d] = math.fsum(wj * float(vr[g, d]) for wj, (_, vr) in zip(w, keys)) / tot
+                out[i, h, d] = math.fsum(wj * float(vr[g, d]) for wj, (_, vr) in zip(w, seen)) / tot
     return out, lse
 
 
@@ -205,6 +208,119 @@ def check_attention_invariants(impl, seed=3):
     o5, _ = impl.denoise_attention_seq(q, impl.context_rows(pk, table, L, ps),
                                        impl.context_rows(pv, table, L, ps), kb, vb, 0.9)
     assert np.array_equal(o5, o)
+
+
+# ------------------------------------------------------------------ causal-block attention pins
+# The context tower taking in a committed block: block query i sees every context key and
+# the block keys 0..i (gist.science summary, "Technisches Resümee — Architektur": the frozen
+# tower is causal over the prompt and the committed tokens).
+
+def check_causal_block_bruteforce(impl, seed=7):
+    rng = np.random.default_rng(seed)
+    ps = 4
+    for L in (0, 1, 3, 5, 9):
+        S, Hq, Hkv, D = 4, 4, 2, 3
+        q = rng.normal(size=(S, Hq, D))
+        ctx_k, ctx_v = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+        kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+        pk, table = _paged_from_contiguous(rng, ctx_k, ps)
+        pv = np.full_like(pk, np.nan)
+        for j in range(L):
+            pv[table[j // ps], :, j % ps, :] = ctx_v[j]
+        want, want_lse = _brute_attention(q, pk, pv, table, L, ps, kb, vb, 0.8, causal_block=True)
+        got, got_lse = impl.denoise_attention_seq(q, impl.context_rows(pk, table, L, ps),
+                                                  impl.context_rows(pv, table, L, ps), kb, vb, 0.8,
+                                                  causal_block=True)
+        assert np.allclose(got, want, rtol=0, atol=1e-12), (L, np.abs(got - want).max())
+        assert np.allclose(got_lse, want_lse, rtol=0, atol=1e-12), (L, np.abs(got_lse - want_lse).max())
+
+
+def check_causal_block_sdpa(impl, seed=8):
+    """With no context the view is PyTorch's causal SDPA (is_causal=True); with a context,
+    block query i is plain SDPA of that one query over [context ; block keys 0..i]."""
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D = 16, 8, 2, 16
+    scale = 1.0 / math.sqrt(D)
+    G = Hq // Hkv
+    q = rng.normal(size=(S, Hq, D))
+    kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+    empty = np.zeros((0, Hkv, D))
+    got, _ = impl.denoise_attention_seq(q, empty, empty, kb, vb, scale, causal_block=True)
+    qt = torch.from_numpy(np.ascontiguousarray(q.transpose(1, 0, 2)))
+    kt = torch.from_numpy(np.ascontiguousarray(kb.transpose(1, 0, 2))).repeat_interleave(G, 0)
+    vt = torch.from_numpy(np.ascontiguousarray(vb.transpose(1, 0, 2))).repeat_interleave(G, 0)
+    want = torch.nn.functional.scaled_dot_product_attention(qt[None], kt[None], vt[None], scale=scale,
+                                                            is_causal=True)[0].numpy().transpose(1, 0, 2)
+    assert np.allclose(got, want, rtol=0, atol=1e-12), np.abs(got - want).max()
+    for L in (1, 21, 64):
+        ctx_k, ctx_v = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+        got, _ = impl.denoise_attention_seq(q, ctx_k, ctx_v, kb, vb, scale, causal_block=True)
+        for i in range(S):
+            want_i = _sdpa(q[i:i + 1], np.concatenate([ctx_k, kb[:i + 1]]),
+                           np.concatenate([ctx_v, vb[:i + 1]]), scale, G)
+            assert np.allclose(got[i:i + 1], want_i, rtol=0, atol=1e-12), (L, i)
+
+
+def check_causal_block_closed_forms(impl, seed=9):
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D = 5, 4, 2, 6
+    G = Hq // Hkv
+    q = rng.normal(size=(S, Hq, D))
+    vb = rng.normal(size=(S, Hkv, D))
+    kb = rng.normal(size=(S, Hkv, D))
+    empty = np.zeros((0, Hkv, D))
+    # (1) no context: block query 0 sees only block key 0 -> exactly its V row, lse = its score
+    o, lse = impl.denoise_attention_seq(q, empty, empty, kb, vb, 0.6, causal_block=True)
+    for h in range(Hq):
+        assert np.array_equal(o[0, h], vb[0, h // G])
+        assert math.isclose(lse[h, 0], 0.6 * float(q[0, h] @ kb[0, h // G]), rel_tol=0, abs_tol=1e-13)
+    # (2) all keys equal -> block query i averages V over the L + i + 1 keys it sees
+    L = 7
+    k_all = rng.normal(size=(Hkv, D))
+    kc = np.broadcast_to(k_all, (L, Hkv, D)).copy()
+    kbe = np.broadcast_to(k_all, (S, Hkv, D)).copy()
+    vc = rng.normal(size=(L, Hkv, D))
+    o, lse = impl.denoise_attention_seq(q, kc, vc, kbe, vb, 0.6, causal_block=True)
+    allv = np.concatenate([vc, vb])
+    for i in range(S):
+        mean_v = allv[:L + i + 1].mean(axis=0)
+        for h in range(Hq):
+            assert np.allclose(o[i, h], mean_v[h // G], rtol=0, atol=1e-12), (i, h)
+            c = 0.6 * float(q[i, h] @ k_all[h // G])
+            assert math.isclose(lse[h, i], c + math.log(L + i + 1), rel_tol=0, abs_tol=1e-12)
+
+
+def check_causal_block_invariants(impl, seed=10):
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D, L = 6, 4, 1, 5, 9
+    q = rng.normal(size=(S, Hq, D))
+    kc, vc = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+    kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+    o, lse = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.7, causal_block=True)
+    ob, lseb = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.7)
+    # the last block position sees everything: same as the bidirectional view
+    assert np.allclose(o[-1], ob[-1], rtol=0, atol=1e-14) and np.allclose(lse[:, -1], lseb[:, -1], rtol=0,
+                                                                           atol=1e-14)
+    # earlier positions do not (the later block keys carry weight in the bidirectional view)
+    assert (np.abs(o[:-1] - ob[:-1]).max(axis=(1, 2)) > 1e-6).all()
+    # a later block key or value never reaches an earlier query: bitwise unchanged rows
+    for j in range(S):
+        kb2, vb2 = kb.copy(), vb.copy()
+        kb2[j] += 3.0
+        vb2[j] -= 7.0
+        o2, lse2 = impl.denoise_attention_seq(q, kc, vc, kb2, vb2, 0.7, causal_block=True)
+        assert np.array_equal(o2[:j], o[:j]) and np.array_equal(lse2[:, :j], lse[:, :j]), j
+        assert (np.abs(o2[j:] - o[j:]).max(axis=(1, 2)) > 1e-6).all(), j
+    # a block query that sees its own key dominate returns that key's V row
+    u = rng.normal(size=D)
+    u /= np.linalg.norm(u)
+    q3, kb3 = q * 1e-3, kb * 1e-3
+    kc3 = kc * 1e-3
+    i = 3
+    q3[i, 0] = 10.0 * u
+    kb3[i, 0] = 6.0 * u
+    o3, _ = impl.denoise_attention_seq(q3, kc3, vc, kb3, vb, 1.0, causal_block=True)
+    assert np.allclose(o3[i, 0], vb[i, 0], rtol=0, atol=1e-15)
 
 
 # ------------------------------------------------------------------ unmasking pins
@@ -385,5 +501,6 @@ def check_append(impl, seed=6):
 
 
 ALL_CHECKS = [check_attention_bruteforce, check_attention_sdpa, check_attention_closed_forms,
-              check_attention_invariants, check_unmask_closed_forms, check_unmask_bruteforce,
+              check_attention_invariants, check_causal_block_bruteforce, check_causal_block_sdpa,
+              check_causal_block_closed_forms, check_causal_block_invariants, check_unmask_closed_forms, check_unmask_bruteforce,
               check_unmask_rules, check_block_loop, check_append]

@@ -12,7 +12,7 @@ from tests import oracle_pins
 
 
 def _attention_mutant(kind):
-    def attn(q, k_ctx, v_ctx, k_blk, v_blk, sm_scale, key_bias=None, return_probs=False):
+    def attn(q, k_ctx, v_ctx, k_blk, v_blk, sm_scale, key_bias=None, return_probs=False, causal_block=False):
         S, Hq, D = q.shape
         Hkv = k_blk.shape[1]
         G = Hq // Hkv
@@ -36,16 +36,31 @@ def _attention_mutant(kind):
             s = sc * (q[:, h, :] @ K[:, g, :].T)
             if key_bias is not None and kind not in ("drop_block", "drop_context"):
                 s = s + key_bias[None, :]
-            if kind == "causal_block":
-                L = k_ctx.shape[0]
+            L = k_ctx.shape[0]
+            if kind == "causal_block" or (causal_block and kind == "none"):
                 for i in range(S):
                     s[i, L + i + 1:] = -np.inf
+            elif causal_block and kind == "causal_strict":      # a query misses its own key
+                for i in range(S):
+                    s[i, L + i:] = -np.inf
+            elif causal_block and kind == "causal_loose":       # one key too many
+                for i in range(S):
+                    s[i, L + i + 2:] = -np.inf
+            elif causal_block and kind == "causal_top_left":    # triangle over [context ; block]
+                for i in range(S):
+                    s[i, i + 1:] = -np.inf
+            elif causal_block and kind == "causal_on_block_values_only":
+                pass                                            # mask applied to P below instead
             m = s.max(axis=1, keepdims=True)
             e = np.exp(s - m)
             if kind == "wrong_axis":
                 p = e / e.sum(axis=0, keepdims=True)
             else:
                 p = e / e.sum(axis=1, keepdims=True)
+            if causal_block and kind == "causal_on_block_values_only":
+                # later block keys dropped after the normalisation (weights no longer sum to 1)
+                for i in range(S):
+                    p[i, L + i + 1:] = 0.0
             src = K if kind == "k_for_v" else Vv
             o[:, h, :] = p @ src[:, g, :]
             z = e.sum(axis=1)
@@ -155,7 +170,8 @@ def _impl(**override):
 MUTANTS = (
     [("attn_" + k, dict(denoise_attention_seq=_attention_mutant(k)))
      for k in ("gqa_modulo", "drop_block", "drop_context", "no_scale", "wrong_axis", "k_for_v",
-               "lse_no_max", "causal_block")]
+               "lse_no_max", "causal_block", "causal_ignored", "causal_strict", "causal_loose",
+               "causal_top_left", "causal_on_block_values_only")]
     + [("rows_" + k, dict(context_rows=_context_rows_mutant(k)))
        for k in ("slot_off_by_one", "physical_order")]
     + [("unmask_" + k, dict(unmask_seq=_unmask_mutant(k)))
