@@ -140,6 +140,22 @@ def tt_denoise_attn(cache: KVCache, q: torch.Tensor, k_blk: torch.Tensor, v_blk:
                     ws: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Two-segment attention of one layer; q [B,S,Hq,D], k_blk/v_blk [B,S,Hkv,D] -> out [B,S,Hq,D]."""
+    return _attention("tt_denoise_attn", cache, q, k_blk, v_blk, out, lse, sm_scale, max_ctas, ws, dev_err,
+                      stream)
+
+
+def tt_context_block_attn(cache: KVCache, q: torch.Tensor, k_blk: torch.Tensor, v_blk: torch.Tensor,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          sm_scale: Optional[float] = None, max_ctas: int = 0,
+                          ws: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The context tower's attention over a committed block: as tt_denoise_attn, but block
+    query i sees block keys 0..i only."""
+    return _attention("tt_context_block_attn", cache, q, k_blk, v_blk, out, lse, sm_scale, max_ctas, ws,
+                      dev_err, stream)
+
+
+def _attention(name, cache, q, k_blk, v_blk, out, lse, sm_scale, max_ctas, ws, dev_err, stream):
     B, S, Hq, D = q.shape
     Hkv = cache.n_kv_heads
     _need(q, "q", cache.dtype)
@@ -156,10 +172,10 @@ def tt_denoise_attn(cache: KVCache, q: torch.Tensor, k_blk: torch.Tensor, v_blk:
     if ws is None:
         ws = workspace(tt_denoise_attn_workspace_size(B, S, Hq, Hkv, D, cache.dtype), q.device)
     st = cache.struct()
-    N.check(N.lib().tt_denoise_attn(ctypes.byref(st), q.data_ptr(), k_blk.data_ptr(), v_blk.data_ptr(),
-                                    out.data_ptr(), _ptr(lse), B, S, Hq, float(sm_scale), int(max_ctas),
-                                    ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
-            "tt_denoise_attn")
+    N.check(getattr(N.lib(), name)(ctypes.byref(st), q.data_ptr(), k_blk.data_ptr(), v_blk.data_ptr(),
+                                   out.data_ptr(), _ptr(lse), B, S, Hq, float(sm_scale), int(max_ctas),
+                                   ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+            name)
     return out
 
 

@@ -5,7 +5,9 @@
 // Architektur"; dgnews.ru, "How the architecture actually works"): a block
 // query attends to every key the context tower holds for its layer (all of them
 // precede the block, so the causal cross-attention admits them all) and,
-// without a mask, to every key of its own block.
+// without a mask, to every key of its own block.  In the context tower's view of
+// a committed block (causal_block; the same summary: that tower is causal over
+// the committed tokens) block query i reads the block keys 0..i only.
 //
 // One warp owns one (sequence, block position, query head) row.  Each lane
 // holds D/32 consecutive dimensions, so a key or value row is one coalesced
@@ -34,6 +36,7 @@ struct SimtParams {
     float *lse;
     int B, S, Hq, Hkv, G;
     float sm_scale;
+    int causal_block;
     uint32_t *dev_err;
 };
 
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) attn_simt_kernel(const Simt
 #pragma unroll
     for (int d = 0; d < DPL; ++d) o[d] = 0.f;
     bool bad = false;
-    const int n_keys = L + p.S;
+    const int n_keys = L + (p.causal_block ? i + 1 : p.S);
     for (int j0 = 0; j0 < n_keys; j0 += 4) {
         float s[4];
         float v[4][DPL];
@@ -196,6 +199,7 @@ tt_status launch_attn_simt(const AttnArgs &a) {
     p.q = a.q; p.k_blk = a.k_blk; p.v_blk = a.v_blk; p.out = a.out; p.lse = a.lse;
     p.B = a.B; p.S = a.S; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = a.Hq / a.Hkv;
     p.sm_scale = a.sm_scale;
+    p.causal_block = a.causal_block ? 1 : 0;
     p.dev_err = a.dev_err;
     if (p.B == 0) return TT_OK;
     return a.ctx->dtype == TT_BF16 ? launch_typed<uint16_t>(p, a.D, a.stream)

@@ -5,7 +5,10 @@
 // Architektur" and "Generierungsprozess"; dgnews.ru, "How the architecture
 // actually works"): the S block queries of every query head attend, in one
 // softmax, to all L context keys the frozen context tower holds for this layer
-// and to the S keys of their own block, without a mask inside the block.
+// and to the S keys of their own block, without a mask inside the block.  In the
+// context tower's view of a committed block (causal_block: the same summary makes
+// that tower causal over the committed tokens) block query i reads block keys
+// 0..i only; the kernel is the same but for that mask on the block tile.
 //
 // Design for sm_103a:
 //  * Rows.  The G = Hq/Hkv query heads of one KV head share every key, so the
@@ -121,6 +124,7 @@ struct TcParams {
     int B, S, Hq, Hkv, G, rows;
     int cps;                             // CTAs per segment (M tiles): 1 or 2
     float scale_log2;
+    int causal_block;                    // block tile: row (s, head) sees block keys 0..s
     int n_groups;
     unsigned *tickets;                   // [segment][M tile]
     float *part;
@@ -662,7 +666,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
             for (int j = 0; j < ntiles; ++j, ++t) {
                 if ((t & 1) != h) continue;              // the partner's tile
                 const int sb = h;                        // P buffer of this tile
-                const int valid = tile_valid(pc, pc.first + j, S);
+                int valid = tile_valid(pc, pc.first + j, S);
+                if (p.causal_block && pc.first + j == pc.ntc) valid = s_pos + 1;   // per row
                 if (!wait_bar(sh, &bar.s_full[h], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t scol = tmem + lane_off + kColS;
@@ -677,7 +682,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.s_empty);
-                if (valid < kTileKeys) {   // warp-uniform
+                if (valid < kTileKeys) {   // warp-uniform, except on a causal block tile
                     mask_scores(a0, 0, valid);
                     mask_scores(a1, 32, valid);
                     mask_scores(a2, 64, valid);
@@ -976,6 +981,7 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     p.lse = a.lse ? a.lse + (size_t)b0 * a.Hq * a.S : nullptr;
     p.B = nb; p.S = a.S; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rows = rows; p.cps = cps;
     p.scale_log2 = a.sm_scale * kLog2e;
+    p.causal_block = a.causal_block ? 1 : 0;
     int n = a.max_ctas > 0 ? a.max_ctas : sms;
     if (n > kMaxCtas) n = kMaxCtas;
     const int n_groups = n / cps > 0 ? n / cps : 1;

@@ -67,10 +67,15 @@ tt_status tt_denoise_attn_workspace_size(int B, int S, int Hq, int Hkv, int D, t
     return TT_OK;
 }
 
-tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const void *k_blk,
-                          const void *v_blk, void *out, float *lse, int B, int S, int Hq,
-                          float sm_scale, int max_ctas, void *ws, size_t ws_bytes,
-                          uint32_t *dev_err, tt_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The two attention entry points differ only in the view inside the block.
+tt_status attention(const tt_kv_cache *ctx, const void *q, const void *k_blk, const void *v_blk,
+                    void *out, float *lse, int B, int S, int Hq, float sm_scale, int max_ctas,
+                    void *ws, size_t ws_bytes, uint32_t *dev_err, tt_stream_t stream,
+                    bool causal_block) {
     tt_status st = check_cache(ctx);
     if (st != TT_OK) return st;
     st = attn_shape(B, S, Hq, ctx->n_kv_heads, ctx->head_dim, ctx->dtype);
@@ -82,7 +87,8 @@ tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const void *k_b
     AttnArgs a;
     a.ctx = ctx; a.q = q; a.k_blk = k_blk; a.v_blk = v_blk; a.out = out; a.lse = lse;
     a.B = B; a.S = S; a.Hq = Hq; a.Hkv = ctx->n_kv_heads; a.D = ctx->head_dim;
-    a.sm_scale = sm_scale; a.max_ctas = max_ctas; a.ws = ws; a.ws_bytes = ws_bytes;
+    a.sm_scale = sm_scale; a.causal_block = causal_block;
+    a.max_ctas = max_ctas; a.ws = ws; a.ws_bytes = ws_bytes;
     a.dev_err = dev_err; a.stream = reinterpret_cast<cudaStream_t>(stream);
     if (attn_tc_supported(S, Hq, a.Hkv, a.D, ctx->page_size, (tt_dtype)ctx->dtype) && sm_scale > 0.f) {
         const size_t need = attn_tc_ws_bytes(B, S, Hq, a.Hkv, a.D);
@@ -91,6 +97,26 @@ tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const void *k_b
         return launch_attn_tc(a);
     }
     return launch_attn_simt(a);
+}
+
+}  // namespace
+
+extern "C" {
+
+tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const void *k_blk,
+                          const void *v_blk, void *out, float *lse, int B, int S, int Hq,
+                          float sm_scale, int max_ctas, void *ws, size_t ws_bytes,
+                          uint32_t *dev_err, tt_stream_t stream) {
+    return attention(ctx, q, k_blk, v_blk, out, lse, B, S, Hq, sm_scale, max_ctas, ws, ws_bytes,
+                     dev_err, stream, false);
+}
+
+tt_status tt_context_block_attn(const tt_kv_cache *ctx, const void *q, const void *k_blk,
+                                const void *v_blk, void *out, float *lse, int B, int S, int Hq,
+                                float sm_scale, int max_ctas, void *ws, size_t ws_bytes,
+                                uint32_t *dev_err, tt_stream_t stream) {
+    return attention(ctx, q, k_blk, v_blk, out, lse, B, S, Hq, sm_scale, max_ctas, ws, ws_bytes,
+                     dev_err, stream, true);
 }
 
 tt_status tt_unmask_workspace_size(int B, int S, int V, tt_dtype dtype, size_t *bytes) {

@@ -44,6 +44,7 @@ struct AttnArgs {
     float *lse;
     int B, S, Hq, Hkv, D;
     float sm_scale;
+    bool causal_block;   // block query i sees block keys 0..i only (else all S)
     int max_ctas;
     void *ws;
     size_t ws_bytes;

@@ -3,6 +3,8 @@
  *
  * One denoiser step of block-wise diffusion decoding on one GPU:
  *   tt_denoise_attn  two-segment attention of the S block queries of one layer
+ *   tt_context_block_attn  the same attention with a causal view inside the
+ *                    block: the context tower taking in a committed block
  *   tt_unmask        confidence unmasking of the block over the vocabulary logits
  *   tt_kv_append     commit of a finished block's KV into the context caches
  *   tt_block_step    all attention layers of one step followed by the unmasking
@@ -154,6 +156,25 @@ TT_API tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const vo
                           const void *v_blk, void *out, float *lse, int B, int S, int Hq,
                           float sm_scale, int max_ctas, void *ws, size_t ws_bytes,
                           uint32_t *dev_err, tt_stream_t stream);
+
+/* Attention of the frozen context tower over a committed block ([ARCH]: that
+ * tower is a causal autoregressive model over the prompt and the committed
+ * tokens; [GEN]: once a block is committed, the tower extends its state with
+ * the clean block).
+ *
+ * Identical to tt_denoise_attn -- arguments, layouts, workspace (sized by
+ * tt_denoise_attn_workspace_size), supported shapes, kernels and errors --
+ * except for the view inside the block, which is causal:
+ *   keys of block query i = the L = ctx_len[b] context keys, then the block
+ *                           keys 0..i (L + i + 1 keys in all);
+ *   p = softmax(s) over those keys;  out and lse as in tt_denoise_attn.
+ * q, k_blk and v_blk are the context tower's projections of the block's clean
+ * tokens for this layer; the k_blk and v_blk it attends to are the rows that
+ * tt_kv_append then stores in the cache. */
+TT_API tt_status tt_context_block_attn(const tt_kv_cache *ctx, const void *q, const void *k_blk,
+                                const void *v_blk, void *out, float *lse, int B, int S, int Hq,
+                                float sm_scale, int max_ctas, void *ws, size_t ws_bytes,
+                                uint32_t *dev_err, tt_stream_t stream);
 
 /* Bytes of workspace tt_unmask needs (pure host arithmetic). */
 TT_API tt_status tt_unmask_workspace_size(int B, int S, int V, tt_dtype dtype, size_t *bytes);

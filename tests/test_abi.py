@@ -70,9 +70,10 @@ def _cache(**kw):
     return c
 
 
-def test_attention_rejects_bad_arguments_on_the_host(lib):
+@pytest.mark.parametrize("entry", ["tt_denoise_attn", "tt_context_block_attn"])
+def test_attention_rejects_bad_arguments_on_the_host(lib, entry):
     def call(cache, q=0x10000, B=1, S=16, Hq=32, scale=0.1, max_ctas=0):
-        return lib.tt_denoise_attn(ctypes.byref(cache) if cache is not None else None, q, 0x20000, 0x30000,
+        return getattr(lib, entry)(ctypes.byref(cache) if cache is not None else None, q, 0x20000, 0x30000,
                                    0x40000, None, B, S, Hq, scale, max_ctas, None, 0, None, None)
     assert call(None) == N.TT_ERR_INVALID_ARG
     assert call(_cache(page_table=0)) == N.TT_ERR_INVALID_ARG
