@@ -373,6 +373,11 @@ def run_ours(a, cfg):
         api.tt_denoise_attn(c["cache"], c["q"], c["kb"], c["vb"], out=c["out"], sm_scale=scale, ws=attn_ws,
                             dev_err=err, stream=stream)
 
+    def ctx_attn_only(i, stream=None):
+        c = copies[i % n_copies]
+        api.tt_context_block_attn(c["cache"], c["q"], c["kb"], c["vb"], out=c["out"], sm_scale=scale,
+                                  ws=attn_ws, dev_err=err, stream=stream)
+
     k_ker = max(10, min(a.steps, 200))   # launches per kernel-only timing
     unm_masked = torch.ones((k_ker, cfg.B, cfg.S), dtype=torch.uint8, device=dev)
     unm_tokens = torch.full((k_ker, cfg.B, cfg.S), -1, dtype=torch.int32, device=dev)
@@ -459,6 +464,10 @@ def run_ours(a, cfg):
     attn_ms = timed(attn_only, 0, k_ker, use_graph) / k_ker
     unm_masked.fill_(1)
     unmask_ms = timed(unmask_only, 0, k_ker, use_graph) / k_ker
+    # the context tower's causal view of the same block (not part of the denoise step)
+    ctx_attn_ms = timed(ctx_attn_only, 0, k_ker, use_graph) / k_ker
+    if api.tt_get_device_error(err) != 0:
+        raise SystemExit("device error in the per-kernel timings")
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the region
     e2e = None
@@ -551,6 +560,11 @@ def run_ours(a, cfg):
                 "unmask": {"us": unmask_ms * 1e3, "gbs": unm_gbs, "hbm_frac": unm_gbs / hbm,
                            "roofline_us": ub / (hbm * 1e9) * 1e6,
                            "traffic": profiled_traffic("unmask", cfg.name)},
+                "context_block_attention": {
+                    "us": ctx_attn_ms * 1e3, "gbs": ab / (ctx_attn_ms * 1e-3) / 1e9,
+                    "hbm_frac": ab / (ctx_attn_ms * 1e-3) / 1e9 / hbm,
+                    "roofline_us": max(ab / (hbm * 1e9), af / (tc * 1e12)) * 1e6,
+                    "note": "tt_context_block_attn on the same inputs; timed separately, not in the step"},
                 "step_roofline_us": step_roof_us, "step_frac": step_roof_us / (ms / a.steps * 1e3)},
             "gpu_launches": a.steps * launches_per_step(cfg),
             "graph": use_graph,

@@ -6,9 +6,10 @@
 // actually works"): the S block queries of every query head attend, in one
 // softmax, to all L context keys the frozen context tower holds for this layer
 // and to the S keys of their own block, without a mask inside the block.  In the
-// context tower's view of a committed block (causal_block: the same summary makes
-// that tower causal over the committed tokens) block query i reads block keys
-// 0..i only; the kernel is the same but for that mask on the block tile.
+// context tower's view of a committed block (the same summary makes that tower
+// causal over the committed tokens) block query i reads block keys 0..i only:
+// a second instance of the kernel (kCausal) that masks the block tile per row,
+// so the denoise instance carries no code for it.
 //
 // Design for sm_103a:
 //  * Rows.  The G = Hq/Hkv query heads of one KV head share every key, so the
@@ -124,7 +125,6 @@ struct TcParams {
     int B, S, Hq, Hkv, G, rows;
     int cps;                             // CTAs per segment (M tiles): 1 or 2
     float scale_log2;
-    int causal_block;                    // block tile: row (s, head) sees block keys 0..s
     int n_groups;
     unsigned *tickets;                   // [segment][M tile]
     float *part;
@@ -382,6 +382,7 @@ __device__ __forceinline__ float softmax_chunk(const uint32_t (&sv)[32], uint64_
 // (two warps per TMEM lane quarter taking alternate tiles; at the end of a piece each
 // writes half of the O columns).
 
+template <bool kCausal>
 __global__ void __launch_bounds__(384, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -667,7 +668,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 if ((t & 1) != h) continue;              // the partner's tile
                 const int sb = h;                        // P buffer of this tile
                 int valid = tile_valid(pc, pc.first + j, S);
-                if (p.causal_block && pc.first + j == pc.ntc) valid = s_pos + 1;   // per row
+                if constexpr (kCausal) {
+                    if (pc.first + j == pc.ntc) valid = s_pos + 1;   // block keys 0..s_pos
+                }
                 if (!wait_bar(sh, &bar.s_full[h], ((uint32_t)t >> 1) & 1, p.dev_err)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t scol = tmem + lane_off + kColS;
@@ -682,7 +685,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.s_empty);
-                if (valid < kTileKeys) {   // warp-uniform, except on a causal block tile
+                if (valid < kTileKeys) {   // warp-uniform (per row on a causal block tile)
                     mask_scores(a0, 0, valid);
                     mask_scores(a1, 32, valid);
                     mask_scores(a2, 64, valid);
@@ -981,7 +984,6 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     p.lse = a.lse ? a.lse + (size_t)b0 * a.Hq * a.S : nullptr;
     p.B = nb; p.S = a.S; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rows = rows; p.cps = cps;
     p.scale_log2 = a.sm_scale * kLog2e;
-    p.causal_block = a.causal_block ? 1 : 0;
     int n = a.max_ctas > 0 ? a.max_ctas : sms;
     if (n > kMaxCtas) n = kMaxCtas;
     const int n_groups = n / cps > 0 ? n / cps : 1;
@@ -991,10 +993,10 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     p.part = reinterpret_cast<float *>(static_cast<char *>(a.ws) + align_up((size_t)cps * nseg * sizeof(unsigned), 256));
     p.slot_floats = (long long)rows * kD + 2LL * rows;
     p.dev_err = a.dev_err;
-    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
+    auto kernel = a.causal_block ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
         return TT_ERR_CUDA;
-    attn_tc_kernel<<<n_groups * cps, 384, kSmemBytes, a.stream>>>(mk, mv, mkb, mvb, p);
+    kernel<<<n_groups * cps, 384, kSmemBytes, a.stream>>>(mk, mv, mkb, mvb, p);
     return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
