@@ -52,3 +52,18 @@ def test_unmask_worked_example():
         assert list(r.committed_now.astype(int)) == [int(x) for x in g[f"step{step}_committed"][0].split()]
         masked, tokens = r.masked, r.tokens
     assert list(tokens) == [int(x) for x in g["final_tokens"][0].split()]
+
+
+def test_context_block_attention_worked_example():
+    g = _read("context_block_attention_worked.txt")
+    q = _nums(g["q"])[:, None, :]
+    kc, vc = _nums(g["k_ctx"])[:, None, :], _nums(g["v_ctx"])[:, None, :]
+    kb, vb = _nums(g["k_blk"])[:, None, :], _nums(g["v_blk"])[:, None, :]
+    o, lse = oracle.denoise_attention_seq(q, kc, vc, kb, vb, 1.0, causal_block=True)
+    for i in range(2):
+        want_o = [eval(x, {"__builtins__": {}}, _ENV) for x in g[f"o{i}"]]
+        assert np.allclose(o[i, 0], want_o, rtol=1e-15, atol=0), i
+        assert abs(lse[0, i] - eval(g["lse"][i], {"__builtins__": {}}, _ENV)) < 1e-15, i
+    # the denoise view differs at block position 0 (it also sees k2)
+    ob, _ = oracle.denoise_attention_seq(q, kc, vc, kb, vb, 1.0)
+    assert not np.allclose(ob[0, 0], o[0, 0])
