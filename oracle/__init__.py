@@ -5,4 +5,5 @@ import this package.  The CUDA library never links, imports or executes it,
 and it imports nothing from the library.
 """
 from .twotower import (UnmaskResult, context_rows, decode, denoise_attention,  # noqa: F401
-                       denoise_attention_seq, kv_append, unmask, unmask_seq)
+                       denoise_attention_seq, kv_append, linear_schedule_mask, masked_nll,
+                       masked_nll_seq, unmask, unmask_seq)

@@ -24,6 +24,10 @@ Sources (the pages print no algorithm listing for these steps, only prose):
   confidence is above a threshold gamma are committed, the others stay masked.
   Also "Der Konfidenz-Trick": a confident word is locked at once and never
   revisited; an uncertain one stays masked for the next round.
+* [T] same page, "Training und Konditionierung — Maskierte Diffusion": clean
+  blocks are corrupted by replacing tokens with [MASK] following a linear
+  schedule, and the denoiser minimises the negative log-likelihood of the
+  original tokens at the masked positions.
 * [R] dgnews.ru news article on Nemotron-TwoTower, section "How the
   architecture actually works": inside a block every masked position attends
   to all other block positions; towards earlier blocks and the prompt the
@@ -41,6 +45,11 @@ confidence is the maximum softmax probability at temperature 1; a position is
 committed when conf >= tau; if none qualifies the single most confident
 masked position is committed (lowest position on ties); at step T every
 masked position is committed; argmax ties resolve to the lowest token id.
+On the training side, the linear schedule masks each position independently
+with probability t (it survives with probability 1 - t), the uniform draws are
+inputs, and the loss is the per-position NLL of the clean token at the masked
+positions with its sum and count per sequence (no weight over t: the pages
+state none).
 
 Parity of every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, a library routine for the no-context case, and
@@ -273,3 +282,61 @@ def kv_append(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray, ct
             v_pool[page, :, j % page_size, :] = v_new[b, s]
         new_len[b] = L + S
     return new_len
+
+
+# --------------------------------------------------------------------------- masked-diffusion loss
+
+def linear_schedule_mask(u: np.ndarray, t: float) -> np.ndarray:
+    """Corruption of a clean block at diffusion time t under the linear schedule ([T]).
+
+    Each position is replaced by [MASK] with probability t and kept with
+    probability 1 - t, independently of the others.  The uniform draws u_p in
+    [0, 1) are inputs (one per position); position p is masked iff u_p < t, so
+    P(masked) = t exactly.  t must lie in [0, 1].
+    """
+    if not 0.0 <= t <= 1.0:
+        raise ValueError(f"diffusion time {t} outside [0, 1]")
+    return np.asarray(u, dtype=np.float64) < t
+
+
+def masked_nll_seq(logits: np.ndarray, targets: np.ndarray, masked: np.ndarray):
+    """Negative log-likelihood of the clean tokens at the masked positions of one block ([T]).
+
+    For every masked position p with clean token x_p:
+        nll_p = log sum_v exp(l_{p,v}) - l_{p,x_p}      (= -log softmax(l_p)[x_p]),
+    evaluated with the row maximum taken out first.  Unmasked positions are
+    skipped (their logits are never read) and get NaN.  Returns nll [S], the sum
+    over the masked positions and their count.
+    """
+    S = len(masked)
+    nll = np.full(S, np.nan)
+    total, count = 0.0, 0
+    for p in range(S):
+        if not masked[p]:
+            continue
+        row = np.asarray(logits[p], dtype=np.float64)
+        m = row.max()
+        lse = m + np.log(np.exp(row - m).sum())
+        nll[p] = lse - row[int(targets[p])]
+        total += nll[p]
+        count += 1
+    return nll, total, count
+
+
+def masked_nll(logits: np.ndarray, targets: np.ndarray, masked: np.ndarray, dtype: str,
+               seqs: Optional[Sequence[int]] = None):
+    """Batched masked NLL: logits [B, S, V] as stored; targets, masked [B, S].
+
+    Returns nll [B, S] (NaN where unmasked or outside ``seqs``), per-sequence sums
+    [B] and counts [B] (NaN / -1 outside ``seqs``)."""
+    B, S = masked.shape
+    nll = np.full((B, S), np.nan)
+    sums = np.full(B, np.nan)
+    counts = np.full(B, -1, dtype=np.int64)
+    for b in (range(B) if seqs is None else seqs):
+        lg = np.full((S, logits.shape[2]), np.nan)
+        for p in range(S):
+            if masked[b, p]:
+                lg[p] = decode(logits[b, p], dtype)
+        nll[b], sums[b], counts[b] = masked_nll_seq(lg, targets[b], masked[b])
+    return nll, sums, counts

@@ -1,9 +1,10 @@
 """Checks that pin the float64 oracle to things other than itself.
 
 Each ``check_*`` takes an implementation namespace ``impl`` exposing
-``context_rows``, ``denoise_attention_seq``, ``unmask_seq`` and ``kv_append``
-(the oracle, or a deliberately broken copy of it) and raises AssertionError if
-the implementation disagrees with:
+``context_rows``, ``denoise_attention_seq``, ``unmask_seq``, ``kv_append``,
+``linear_schedule_mask`` and ``masked_nll_seq`` (the oracle, or a deliberately
+broken copy of it) and raises AssertionError if the implementation disagrees
+with:
 
 * brute force (pure-Python loops, a different route to the same definition),
 * a library routine in a case that reduces to it (PyTorch's float64
@@ -500,7 +501,94 @@ def check_append(impl, seed=6):
         raise AssertionError("capacity overflow not detected")
 
 
+# ------------------------------------------------------------------ masked-diffusion loss pins
+# Training side (gist.science summary, "Training und Konditionierung — Maskierte Diffusion"):
+# clean blocks masked on a linear schedule; NLL of the clean tokens at the masked positions.
+
+def check_linear_schedule(impl, seed=11):
+    rng = np.random.default_rng(seed)
+    u = rng.random(200_000)
+    assert not impl.linear_schedule_mask(u, 0.0).any()
+    assert impl.linear_schedule_mask(u, 1.0).all()
+    prev = None
+    for t in (0.05, 0.3, 0.5, 0.9):
+        m = impl.linear_schedule_mask(u, t)
+        # P(masked) = t: the fraction is binomial, within 5 standard deviations of t
+        sd = math.sqrt(t * (1 - t) / u.size)
+        assert abs(m.mean() - t) < 5 * sd, (t, m.mean())
+        if prev is not None:
+            assert (m | ~prev).all()             # a later time masks a superset
+        prev = m
+    try:
+        impl.linear_schedule_mask(u[:4], 1.5)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a time outside [0, 1] was accepted")
+
+
+def check_masked_nll_closed_forms(impl):
+    V, S = 1000, 4
+    # all logits equal: every token has probability 1/V -> nll = log V
+    nll, tot, cnt = impl.masked_nll_seq(np.full((S, V), 2.5), np.array([0, 7, 999, 3]), np.ones(S, bool))
+    assert np.allclose(nll, math.log(V), rtol=0, atol=1e-12) and cnt == S
+    assert math.isclose(tot, S * math.log(V), rel_tol=1e-14)
+    # one spike of height a over zeros: at the target nll = log(e^a + V - 1) - a, elsewhere log(e^a + V - 1)
+    a = 7.0
+    lg = np.zeros((S, V))
+    lg[:, 5] = a
+    tg = np.array([5, 6, 5, 0])
+    nll, _, _ = impl.masked_nll_seq(lg, tg, np.ones(S, bool))
+    z = math.log(math.exp(a) + V - 1)
+    assert np.allclose(nll, [z - a, z, z - a, z], rtol=0, atol=1e-12)
+    # unmasked rows are never read (NaN there) and do not count
+    lg[1] = np.nan
+    lg[3] = np.nan
+    nll, tot, cnt = impl.masked_nll_seq(lg, tg, np.array([True, False, True, False]))
+    assert cnt == 2 and math.isclose(tot, 2 * (z - a), rel_tol=1e-13)
+    assert np.isnan(nll[1]) and np.isnan(nll[3])
+
+
+def check_masked_nll_library(impl, seed=12):
+    """Against PyTorch's float64 cross entropy on the masked rows."""
+    rng = np.random.default_rng(seed)
+    S, V = 16, 300
+    lg = rng.normal(0, 3, size=(S, V))
+    tg = rng.integers(0, V, size=S)
+    mk = rng.random(S) < 0.6
+    nll, tot, cnt = impl.masked_nll_seq(lg, tg, mk)
+    want = torch.nn.functional.cross_entropy(torch.from_numpy(lg[mk]), torch.from_numpy(tg[mk]),
+                                             reduction="none").numpy()
+    assert np.allclose(nll[mk], want, rtol=0, atol=1e-12)
+    assert cnt == int(mk.sum()) and math.isclose(tot, float(want.sum()), rel_tol=1e-13)
+
+
+def check_masked_nll_invariants(impl, seed=13):
+    rng = np.random.default_rng(seed)
+    S, V = 5, 64
+    lg = rng.normal(0, 2, size=(S, V))
+    tg = rng.integers(0, V, size=S)
+    mk = np.ones(S, bool)
+    nll, _, _ = impl.masked_nll_seq(lg, tg, mk)
+    assert (nll >= 0).all()
+    # a constant added to a row changes nothing; very large logits stay finite (the maximum is taken out)
+    nll2, _, _ = impl.masked_nll_seq(lg + 1e4, tg, mk)
+    assert np.allclose(nll2, nll, rtol=0, atol=1e-9)
+    nll3, _, _ = impl.masked_nll_seq(lg * 200.0, tg, mk)
+    assert np.isfinite(nll3).all()
+    # exp(-nll) over every possible clean token of a row sums to 1 (a probability distribution)
+    for p in range(S):
+        probs = [math.exp(-impl.masked_nll_seq(lg[p:p + 1], np.array([v]), np.ones(1, bool))[0][0])
+                 for v in range(V)]
+        assert math.isclose(math.fsum(probs), 1.0, rel_tol=0, abs_tol=1e-13)
+    # brute force with math.fsum on the unshifted values (moderate logits, no overflow)
+    for p in range(S):
+        want = math.log(math.fsum(math.exp(float(x)) for x in lg[p])) - float(lg[p, tg[p]])
+        assert math.isclose(nll[p], want, rel_tol=0, abs_tol=1e-12)
+
+
 ALL_CHECKS = [check_attention_bruteforce, check_attention_sdpa, check_attention_closed_forms,
               check_attention_invariants, check_causal_block_bruteforce, check_causal_block_sdpa,
               check_causal_block_closed_forms, check_causal_block_invariants, check_unmask_closed_forms, check_unmask_bruteforce,
-              check_unmask_rules, check_block_loop, check_append]
+              check_unmask_rules, check_block_loop, check_append, check_linear_schedule,
+              check_masked_nll_closed_forms, check_masked_nll_library, check_masked_nll_invariants]

@@ -67,3 +67,17 @@ def test_context_block_attention_worked_example():
     # the denoise view differs at block position 0 (it also sees k2)
     ob, _ = oracle.denoise_attention_seq(q, kc, vc, kb, vb, 1.0)
     assert not np.allclose(ob[0, 0], o[0, 0])
+
+
+def test_masked_nll_worked_example():
+    g = _read("masked_nll_worked.txt")
+    u = _nums(g["u"])[0]
+    masked = oracle.linear_schedule_mask(u, float(g["t"][0]))
+    assert list(masked.astype(int)) == [int(x) for x in g["masked"][0].split()]
+    lg = _nums(g["logits"])
+    tg = np.array([int(x) for x in g["targets"][0].split()])
+    nll, tot, cnt = oracle.masked_nll_seq(lg, tg, masked)
+    want = [eval(x, {"__builtins__": {}}, _ENV) for x in g["nll"]]
+    assert cnt == 2 and np.isnan(nll[1])
+    assert np.allclose(nll[[0, 2]], want, rtol=0, atol=1e-14)
+    assert abs(tot - sum(want)) < 1e-14

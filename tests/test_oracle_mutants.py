@@ -158,10 +158,55 @@ def _append_mutant(kind):
     return kv_append
 
 
+def _schedule_mutant(kind):
+    def mask(u, t):
+        if not 0.0 <= t <= 1.0:
+            if kind != "no_range_check":
+                raise ValueError(t)
+        u = np.asarray(u, dtype=np.float64)
+        if kind == "inverted":            # keeps with probability t instead of masking
+            return u >= t
+        if kind == "one_minus_t":
+            return u < 1.0 - t
+        if kind == "quadratic":
+            return u < t * t
+        return u < t
+    return mask
+
+
+def _nll_mutant(kind):
+    def nll_seq(logits, targets, masked):
+        S = len(masked)
+        nll = np.full(S, np.nan)
+        total, count = 0.0, 0
+        for p in range(S):
+            if not masked[p] and kind != "include_unmasked":
+                continue
+            row = np.asarray(logits[p], dtype=np.float64)
+            m = 0.0 if kind == "no_max_shift" else row.max()
+            lse = m + np.log(np.exp(row - m).sum())
+            tgt = int(targets[p]) + (1 if kind == "target_off_by_one" else 0)
+            tgt = min(tgt, row.shape[0] - 1)
+            if kind == "wrong_sign":
+                nll[p] = row[tgt] - lse
+            elif kind == "max_not_lse":
+                nll[p] = m - row[tgt]
+            else:
+                nll[p] = lse - row[tgt]
+            total += nll[p]
+            count += 1
+        if kind == "count_all":
+            count = S
+        return nll, total, count
+    return nll_seq
+
+
 def _impl(**override):
     ns = types.SimpleNamespace(context_rows=oracle.context_rows,
                                denoise_attention_seq=oracle.denoise_attention_seq,
-                               unmask_seq=oracle.unmask_seq, kv_append=oracle.kv_append)
+                               unmask_seq=oracle.unmask_seq, kv_append=oracle.kv_append,
+                               linear_schedule_mask=oracle.linear_schedule_mask,
+                               masked_nll_seq=oracle.masked_nll_seq)
     for k, v in override.items():
         setattr(ns, k, v)
     return ns
@@ -179,13 +224,19 @@ MUTANTS = (
                  "fallback_least", "no_token_write", "reread_locked")]
     + [("append_" + k, dict(kv_append=_append_mutant(k)))
        for k in ("ignore_active", "no_capacity_check", "slot_shift", "k_into_v", "no_len_update")]
+    + [("schedule_" + k, dict(linear_schedule_mask=_schedule_mutant(k)))
+       for k in ("inverted", "one_minus_t", "quadratic", "no_range_check")]
+    + [("nll_" + k, dict(masked_nll_seq=_nll_mutant(k)))
+       for k in ("include_unmasked", "no_max_shift", "target_off_by_one", "wrong_sign", "max_not_lse",
+                 "count_all")]
 )
 
 
 def test_unmutated_copy_passes():
     impl = _impl(denoise_attention_seq=_attention_mutant("none"),
                  context_rows=_context_rows_mutant("none"), unmask_seq=_unmask_mutant("none"),
-                 kv_append=_append_mutant("none"))
+                 kv_append=_append_mutant("none"), linear_schedule_mask=_schedule_mutant("none"),
+                 masked_nll_seq=_nll_mutant("none"))
     for check in oracle_pins.ALL_CHECKS:
         check(impl)
 
