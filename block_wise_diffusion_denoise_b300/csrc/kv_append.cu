@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const __grid_consta
     const int b = blockIdx.x;
     if (p.seq_active != nullptr && p.seq_active[b] == 0) return;
     const int L = p.ctx_len[b];
-    if (L < 0 || L + p.S > p.max_pages * p.page_size) {
+    if (L < 0 || (long long)L + p.S > (long long)p.max_pages * p.page_size) {
         if (threadIdx.x == 0) report_error(p.dev_err, L < 0 ? TT_ERR_BOUNDS : TT_ERR_CAPACITY);
         return;
     }

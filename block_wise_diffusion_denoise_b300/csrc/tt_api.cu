@@ -11,6 +11,9 @@ using namespace tt;
 namespace {
 
 constexpr int kMaxS = 1024;
+// Context capacity per sequence: keeps every length sum in the kernels (a length plus a
+// block, a length rounded up to a tile) inside 32-bit integers.
+constexpr long long kMaxCtxTokens = 1LL << 30;
 
 bool dtype_ok(int d) { return d == TT_BF16 || d == TT_FP32; }
 bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
@@ -23,7 +26,7 @@ tt_status check_cache(const tt_kv_cache *c) {
         return TT_ERR_INVALID_ARG;
     if (c->page_table == nullptr || c->ctx_len == nullptr) return TT_ERR_INVALID_ARG;
     if (c->num_pages > 0 && (c->k_pool == nullptr || c->v_pool == nullptr)) return TT_ERR_INVALID_ARG;
-    if ((long long)c->max_pages_per_seq * c->page_size > 0x7fffffffLL) return TT_ERR_UNSUPPORTED;
+    if ((long long)c->max_pages_per_seq * c->page_size > kMaxCtxTokens) return TT_ERR_UNSUPPORTED;
     if (c->num_pages > 0 && (!aligned16(c->k_pool) || !aligned16(c->v_pool))) return TT_ERR_UNSUPPORTED;
     return TT_OK;
 }
@@ -163,6 +166,7 @@ tt_status tt_kv_append(const tt_kv_cache *layers, int n_layers, const void *cons
                        uint32_t *dev_err, tt_stream_t stream) {
     if (layers == nullptr || n_layers < 1 || k_new == nullptr || v_new == nullptr || B < 0 || S < 1)
         return TT_ERR_INVALID_ARG;
+    if (S > kMaxS) return TT_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l) {
         const tt_status st = check_cache(&layers[l]);
         if (st != TT_OK) return st;

@@ -108,7 +108,8 @@ typedef struct {
     const int32_t *page_table;   /* [B, max_pages_per_seq] */
     int32_t *ctx_len;            /* [B]; read by attention, advanced by tt_kv_append */
     int32_t num_pages;
-    int32_t max_pages_per_seq;
+    int32_t max_pages_per_seq;   /* max_pages_per_seq * page_size <= 2^30 tokens, else
+                                    every call returns TT_ERR_UNSUPPORTED */
     int32_t page_size;           /* tokens per page; 64 on the tensor-core path */
     int32_t n_kv_heads;
     int32_t head_dim;
@@ -250,8 +251,11 @@ TT_API tt_status tt_unmask_noalloc(const void *logits, tt_dtype dtype, int B, in
  * page table.  A block that does not fit max_pages_per_seq pages sets
  * TT_ERR_CAPACITY in dev_err and leaves that sequence untouched.
  *
- * layers   host array of n_layers tt_kv_cache structs
- * k_new, v_new  host arrays of n_layers device pointers, each [B, S, Hkv, D]
+ * layers   host array of n_layers tt_kv_cache structs (1 <= n_layers <= 16;
+ *          more return TT_ERR_UNSUPPORTED, as do S > 1024 and rows of D
+ *          elements that are not a multiple of 16 bytes)
+ * k_new, v_new  host arrays of n_layers device pointers, each [B, S, Hkv, D],
+ *          16-byte aligned like the pools
  * seq_active    device [B] uint8 or NULL */
 TT_API tt_status tt_kv_append(const tt_kv_cache *layers, int n_layers, const void *const *k_new,
                        const void *const *v_new, const uint8_t *seq_active, int B, int S,

@@ -81,6 +81,7 @@ def test_attention_rejects_bad_arguments_on_the_host(lib, entry):
     assert call(_cache(page_size=0)) == N.TT_ERR_INVALID_ARG
     assert call(_cache(dtype=5)) == N.TT_ERR_INVALID_ARG
     assert call(_cache(head_dim=80)) == N.TT_ERR_UNSUPPORTED
+    assert call(_cache(max_pages_per_seq=(1 << 24) + 1)) == N.TT_ERR_UNSUPPORTED   # > 2^30 tokens
     assert call(_cache(k_pool=0x1008)) == N.TT_ERR_UNSUPPORTED          # pool not 16-byte aligned
     assert call(_cache(), Hq=31) == N.TT_ERR_INVALID_ARG                # Hq not a multiple of Hkv
     assert call(_cache(), S=0) == N.TT_ERR_INVALID_ARG
@@ -122,6 +123,13 @@ def test_append_rejects_bad_arguments_on_the_host(lib):
     assert lib.tt_kv_append(same, 2, kn, vn, None, 1, 16, None, None) == N.TT_ERR_INVALID_ARG
     assert lib.tt_kv_append(two, 1, N.ptr_array([0]), vn, None, 1, 16, None, None) == N.TT_ERR_INVALID_ARG
     assert lib.tt_kv_append(two, 1, kn, vn, None, 1, 0, None, None) == N.TT_ERR_INVALID_ARG
+    assert lib.tt_kv_append(two, 1, kn, vn, None, 1, 1025, None, None) == N.TT_ERR_UNSUPPORTED
+    many = (N.tt_kv_cache * 17)(*[_cache() for _ in range(17)])
+    kn17, vn17 = N.ptr_array([0x10000] * 17), N.ptr_array([0x20000] * 17)
+    assert lib.tt_kv_append(many, 17, kn17, vn17, None, 1, 16, None, None) == N.TT_ERR_UNSUPPORTED
+    assert lib.tt_kv_append(two, 1, N.ptr_array([0x10008]), vn, None, 1, 16, None, None) == N.TT_ERR_UNSUPPORTED
+    big = (N.tt_kv_cache * 1)(_cache(max_pages_per_seq=(1 << 24) + 1))   # more than 2^30 tokens
+    assert lib.tt_kv_append(big, 1, kn, vn, None, 1, 16, None, None) == N.TT_ERR_UNSUPPORTED
     assert lib.tt_kv_append(two, 1, kn, vn, None, 0, 16, None, None) == N.TT_OK
 
 
