@@ -31,8 +31,10 @@ def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, allow_no
         if allow_none:
             return None
         raise ValueError(f"{name} is required")
-    if not t.is_cuda:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -44,6 +46,25 @@ def _need(t: Optional[torch.Tensor], name: str, dtype=None, shape=None, allow_no
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+def _ws(ws: torch.Tensor):
+    """(pointer, size in bytes) of a caller's workspace tensor."""
+    _need(ws, "ws")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def _cover(cache: "KVCache", B: int) -> None:
+    """The cache's page table and lengths must cover the B sequences of the call."""
+    if cache.ctx_len.shape[0] < B:
+        raise ValueError(f"the cache holds {cache.ctx_len.shape[0]} sequences, the call {B}")
+
+
+def _err(dev_err: Optional[torch.Tensor]) -> Optional[int]:
+    _need(dev_err, "dev_err", torch.int32, allow_none=True)
+    if dev_err is not None and dev_err.numel() < 1:
+        raise ValueError("dev_err must hold at least one int32")
+    return _ptr(dev_err)
 
 
 @dataclasses.dataclass
@@ -158,6 +179,7 @@ def tt_context_block_attn(cache: KVCache, q: torch.Tensor, k_blk: torch.Tensor, 
 def _attention(name, cache, q, k_blk, v_blk, out, lse, sm_scale, max_ctas, ws, dev_err, stream):
     B, S, Hq, D = q.shape
     Hkv = cache.n_kv_heads
+    _cover(cache, B)
     _need(q, "q", cache.dtype)
     _need(k_blk, "k_blk", cache.dtype, (B, S, Hkv, D))
     _need(v_blk, "v_blk", cache.dtype, (B, S, Hkv, D))
@@ -165,16 +187,16 @@ def _attention(name, cache, q, k_blk, v_blk, out, lse, sm_scale, max_ctas, ws, d
         out = torch.empty_like(q)
     _need(out, "out", cache.dtype, q.shape)
     _need(lse, "lse", torch.float32, (B, Hq, S), allow_none=True)
-    if dev_err is not None:
-        _need(dev_err, "dev_err", torch.int32)
+    err = _err(dev_err)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if ws is None:
         ws = workspace(tt_denoise_attn_workspace_size(B, S, Hq, Hkv, D, cache.dtype), q.device)
+    wp, wb = _ws(ws)
     st = cache.struct()
     N.check(getattr(N.lib(), name)(ctypes.byref(st), q.data_ptr(), k_blk.data_ptr(), v_blk.data_ptr(),
                                    out.data_ptr(), _ptr(lse), B, S, Hq, float(sm_scale), int(max_ctas),
-                                   ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+                                   wp, wb, err, _stream(stream)),
             name)
     return out
 
@@ -193,11 +215,13 @@ def tt_unmask(logits: torch.Tensor, masked: torch.Tensor, tokens: torch.Tensor, 
     _need(committed_now, "committed_now", torch.uint8, (B, S), allow_none=True)
     _need(conf, "conf", torch.float32, (B, S), allow_none=True)
     _need(n_masked, "n_masked", torch.int32, (B,), allow_none=True)
+    err = _err(dev_err)
     if ws is None:
         ws = workspace(tt_unmask_workspace_size(B, S, V, logits.dtype), logits.device)
+    wp, wb = _ws(ws)
     N.check(N.lib().tt_unmask(logits.data_ptr(), _DT[logits.dtype], B, S, V, float(tau), int(step), int(T),
                               masked.data_ptr(), tokens.data_ptr(), _ptr(committed_now), _ptr(conf),
-                              _ptr(n_masked), ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+                              _ptr(n_masked), wp, wb, err, _stream(stream)),
             "tt_unmask")
 
 
@@ -218,9 +242,10 @@ def tt_unmask_noalloc(logits: torch.Tensor, masked: torch.Tensor, tokens: torch.
     _need(committed_now, "committed_now", torch.uint8, (B, S), allow_none=True)
     _need(conf, "conf", torch.float32, (B, S), allow_none=True)
     _need(n_masked, "n_masked", torch.int32, (B,), allow_none=True)
+    err = _err(dev_err)
     N.check(N.lib().tt_unmask_noalloc(logits.data_ptr(), _DT[logits.dtype], B, S, V, float(tau), int(step),
                                       int(T), masked.data_ptr(), tokens.data_ptr(), _ptr(committed_now),
-                                      _ptr(conf), _ptr(n_masked), _ptr(dev_err), _stream(stream)),
+                                      _ptr(conf), _ptr(n_masked), err, _stream(stream)),
             "tt_unmask_noalloc")
 
 
@@ -237,10 +262,13 @@ def tt_kv_append(caches: Sequence[KVCache], k_new: Sequence[torch.Tensor], v_new
         _need(k_new[l], f"k_new[{l}]", caches[l].dtype, shp)
         _need(v_new[l], f"v_new[{l}]", caches[l].dtype, shp)
     _need(seq_active, "seq_active", torch.uint8, (B,), allow_none=True)
+    for c in caches:
+        _cover(c, B)
+    err = _err(dev_err)
     structs = (N.tt_kv_cache * n)(*[c.struct() for c in caches])
     N.check(N.lib().tt_kv_append(structs, n, N.ptr_array([t.data_ptr() for t in k_new]),
                                  N.ptr_array([t.data_ptr() for t in v_new]), _ptr(seq_active), B, S,
-                                 _ptr(dev_err), _stream(stream)),
+                                 err, _stream(stream)),
             "tt_kv_append")
 
 
@@ -259,6 +287,7 @@ def tt_block_step(caches: Sequence[KVCache], q: Sequence[torch.Tensor], k_blk: S
     V = logits.shape[2]
     dt = caches[0].dtype
     for l in range(n):
+        _cover(caches[l], B)
         _need(q[l], f"q[{l}]", dt, (B, S, Hq, D))
         _need(k_blk[l], f"k_blk[{l}]", dt, (B, S, caches[l].n_kv_heads, D))
         _need(v_blk[l], f"v_blk[{l}]", dt, (B, S, caches[l].n_kv_heads, D))
@@ -266,10 +295,15 @@ def tt_block_step(caches: Sequence[KVCache], q: Sequence[torch.Tensor], k_blk: S
     _need(logits, "logits", dt, (B, S, V))
     _need(masked, "masked", torch.uint8, (B, S))
     _need(tokens, "tokens", torch.int32, (B, S))
+    _need(committed_now, "committed_now", torch.uint8, (B, S), allow_none=True)
+    _need(conf, "conf", torch.float32, (B, S), allow_none=True)
+    _need(n_masked, "n_masked", torch.int32, (B,), allow_none=True)
+    err = _err(dev_err)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if ws is None:
         ws = workspace(tt_block_step_workspace_size(B, S, Hq, caches[0].n_kv_heads, D, V, dt), logits.device)
+    wp, wb = _ws(ws)
     structs = (N.tt_kv_cache * n)(*[c.struct() for c in caches])
     N.check(N.lib().tt_block_step(structs, n, N.ptr_array([t.data_ptr() for t in q]),
                                   N.ptr_array([t.data_ptr() for t in k_blk]),
@@ -277,13 +311,14 @@ def tt_block_step(caches: Sequence[KVCache], q: Sequence[torch.Tensor], k_blk: S
                                   N.ptr_array([t.data_ptr() for t in out]), logits.data_ptr(), B, S, Hq, V,
                                   float(tau), int(step), int(T), float(sm_scale), masked.data_ptr(),
                                   tokens.data_ptr(), _ptr(committed_now), _ptr(conf), _ptr(n_masked),
-                                  ws.data_ptr(), ws.numel(), _ptr(dev_err), _stream(stream)),
+                                  wp, wb, err, _stream(stream)),
             "tt_block_step")
 
 
 def tt_get_device_error(dev_err: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream and return the device error word (0 = no error)."""
     code = ctypes.c_uint32(0)
+    _need(dev_err, "dev_err", torch.int32)
     N.check(N.lib().tt_get_device_error(dev_err.data_ptr(), _stream(stream), ctypes.byref(code)),
             "tt_get_device_error")
     return int(code.value)

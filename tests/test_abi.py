@@ -156,3 +156,27 @@ def test_wait_self_check_rejects_bad_arguments_on_the_host(lib):
     assert lib.tt_check_wait_timeout(0, fake, None) == N.TT_ERR_INVALID_ARG
     assert lib.tt_check_wait_timeout((1 << 24) + 1, fake, None) == N.TT_ERR_INVALID_ARG
     assert lib.tt_check_wait_timeout(100, None, None) == N.TT_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """Without the built library every call raises: there is no fallback implementation."""
+    monkeypatch.setattr(N, "_lib", None)
+    monkeypatch.setattr(N, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libtt_denoise.so"))
+    with pytest.raises(N.NativeLibraryMissing):
+        N.lib()
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    torch = pytest.importorskip("torch")
+    from block_wise_diffusion_denoise_b300 import api
+    logits = torch.zeros((1, 16, 64), dtype=torch.bfloat16)
+    masked = torch.ones((1, 16), dtype=torch.uint8)
+    tokens = torch.zeros((1, 16), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.tt_unmask(logits, masked, tokens, 0.9, 1, 4)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.tt_unmask_noalloc(logits, masked, tokens, 0.9, 1, 4)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.KVCache(torch.zeros((2, 1, 64, 128), dtype=torch.bfloat16),
+                    torch.zeros((2, 1, 64, 128), dtype=torch.bfloat16),
+                    torch.zeros((1, 2), dtype=torch.int32), torch.zeros(1, dtype=torch.int32))
