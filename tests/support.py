@@ -63,12 +63,28 @@ def compare_unmask(pre_masked, pre_tokens, ora, gpu_masked, gpu_tokens, gpu_comm
     such a position could decide whether the commit set is empty (every other masked
     position is below tau), the whole sequence is excluded, and so is a sequence whose
     fallback choice is a near tie.  Committed tokens are always compared (the argmax
-    is exact on both sides).  Returns (excluded positions, excluded sequences)."""
+    is exact on both sides).  A sequence whose oracle entry is None (not sampled) gets the
+    checks that need no oracle: only masked positions commit, locked ones never change, at
+    least one position commits while any is masked, everything commits at step T, and the
+    count of positions left matches the mask.  Returns (excluded positions, excluded sequences)."""
     B, S = pre_masked.shape
     ex_pos = ex_seq = 0
     for b in range(B):
         r = ora[b]
         m0 = pre_masked[b].astype(bool)
+        if r is None:
+            com = gpu_committed[b].astype(bool)
+            assert not (com & ~m0).any(), (b, "committed a locked position")
+            assert np.array_equal(gpu_tokens[b][~m0], pre_tokens[b][~m0])
+            assert np.array_equal(gpu_masked[b].astype(bool), m0 & ~com), b
+            assert (gpu_tokens[b][com] >= 0).all()
+            assert np.isnan(gpu_conf[b][~m0]).all() and np.isfinite(gpu_conf[b][m0]).all()
+            if m0.any():
+                assert com.any(), (b, "nothing committed")
+            if step >= T:
+                assert np.array_equal(com, m0)
+            assert gpu_nmasked[b] == int(gpu_masked[b].sum())
+            continue
         # the argmax of every committed position is exact on both sides
         for p in np.nonzero(gpu_committed[b])[0]:
             assert m0[p], (b, p, "committed a locked position")

@@ -16,15 +16,18 @@ from tests import support
 pytestmark = pytest.mark.gpu
 
 
-def _run_loop(cfg, lens, seed, peak_hi):
+def _run_loop(cfg, lens, seed, peak_hi, sample=None):
+    """Runs the loop; checks everything against the oracle, or with ``sample`` (a function of
+    (block, step) returning ([(layer, sequence), ...] for attention, [sequence, ...] for the
+    unmasking)) only those, plus the rules' oracle-free checks on every sequence."""
     L = cfg.n_layers
     cap = int(lens.max()) + cfg.S * (cfg.n_blocks + 1)
     caches = [synth.draw_paged_cache(cfg, lens, cap, seed=seed, layer=l) for l in range(L)]
     devs = [support.cache_to_dev(c) for c in caches]
     for d in devs[1:]:
         d.ctx_len = devs[0].ctx_len                      # the layers hold the same tokens
-    kp = [c.k_pool.copy() for c in caches]               # the oracle's copy of every layer's cache
-    vp = [c.v_pool.copy() for c in caches]
+    kp = [c.k_pool for c in caches]                      # the oracle's copy of every layer's cache
+    vp = [c.v_pool for c in caches]                      # (the device holds its own copy)
     ctx = caches[0].ctx_len.copy()
     scale = 1.0 / math.sqrt(cfg.D)
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
@@ -48,14 +51,24 @@ def _run_loop(cfg, lens, seed, peak_hi):
                               support.to_dev(lg, cfg.dtype), masked, tokens, cfg.tau, step, cfg.T,
                               sm_scale=scale, committed_now=com, conf=conf, n_masked=nm, ws=ws, dev_err=err)
             assert api.tt_get_device_error(err) == 0
-            # every layer's attention against the oracle on the current caches
-            for l in range(L):
+            # attention against the oracle on the current caches (every layer and sequence, or
+            # the sampled ones)
+            tol = 2e-2 if cfg.dtype == "bf16" else 1e-5
+            if sample is None:
+                attn_pairs, unmask_seqs = [(l, None) for l in range(L)], None
+            else:
+                attn_pairs, unmask_seqs = sample(blk, step)
+            for l, b in attn_pairs:
                 want, _ = oracle.denoise_attention(kp[l], vp[l], caches[l].page_table, ctx, cfg.page_size,
-                                                   qkv[l][0], qkv[l][1], qkv[l][2], scale, cfg.dtype)
+                                                   qkv[l][0], qkv[l][1], qkv[l][2], scale, cfg.dtype,
+                                                   seqs=None if b is None else [b])
                 got = support.to_host_f64(outs[l], cfg.dtype)
-                assert support.max_abs(got, want) <= (2e-2 if cfg.dtype == "bf16" else 1e-5), (blk, step, l)
+                if b is None:
+                    assert support.max_abs(got, want) <= tol, (blk, step, l)
+                else:
+                    assert support.max_abs(got[b], want[b]) <= tol, (blk, step, l, b)
             # the unmasking against the oracle from the GPU's pre-step state
-            ora = oracle.unmask(lg, pre_m, pre_t, cfg.tau, step, cfg.T, cfg.dtype)
+            ora = oracle.unmask(lg, pre_m, pre_t, cfg.tau, step, cfg.T, cfg.dtype, seqs=unmask_seqs)
             support.compare_unmask(pre_m, pre_t, ora, masked.cpu().numpy(), tokens.cpu().numpy(),
                                    com.cpu().numpy(), conf.cpu().numpy(), nm.cpu().numpy(), cfg.tau, step,
                                    cfg.T)
@@ -83,6 +96,22 @@ def test_block_loop_bf16_in_lockstep(peak_hi):
     cfg = synth.CONFIGS["loop"].replace(B=3, n_layers=3, T=4, n_blocks=3, V=8192, len_lo=100, len_hi=700)
     lens = np.array([100, 420, 700], np.int32)
     assert _run_loop(cfg, lens, seed=3, peak_hi=peak_hi) >= cfg.n_blocks
+
+
+def test_full_size_block_loop_sampled():
+    """The loop workload at its full size -- 16 sequences of 16384 context tokens, 6 attention
+    layers with their own caches, T = 16, 8 consecutive blocks, V = 131072 -- through the C ABI.
+    At every step one (layer, sequence) attention segment and the unmasking of two sequences
+    are checked against the oracle; every sequence gets the rules' oracle-free checks, every
+    block must finish within T steps, and the lengths grow by one block per commit."""
+    cfg = synth.CONFIGS["loop"]
+    lens = synth.draw_lengths(cfg, 0)
+
+    def sample(blk, step):
+        i = blk * cfg.T + step
+        return [(i % cfg.n_layers, (7 * i) % cfg.B)], sorted({(5 * i) % cfg.B, (5 * i + 3) % cfg.B})
+
+    assert _run_loop(cfg, lens, seed=11, peak_hi=12.0, sample=sample) >= cfg.n_blocks
 
 
 def test_block_loop_fp32_in_lockstep():
