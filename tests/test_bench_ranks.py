@@ -66,3 +66,27 @@ def test_reference_arm_prints_on_rank_zero_only(capsys, monkeypatch):
     assert b.main() == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_line_keeps_the_contract(capsys, monkeypatch):
+    """Every key of the JSON line, with the reference arm's own cpu_baseline and e2e."""
+    b = _bench()
+    monkeypatch.setenv("RANK", "0")
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--config", "single", "--steps", "2",
+                                      "--warmup", "1"])
+    assert b.main() == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert key in line, key
+    assert line["metric"] == b.METRIC and line["unit"] == "steps/s" and line["higher_is_better"] is True
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["scaling"] == "weak" and line["vs_baseline"] is None and line["dtype"] == "f64"
+    assert line["ms_per_step"] == pytest.approx(1e3 / line["value"])
+    assert line["config"]["workload"].startswith("single:")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == "steps/s"
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
