@@ -209,3 +209,13 @@ def test_tensor_core_shapes_beyond_two_m_tiles(S, Hq, Hkv):
     cfg = synth.CONFIGS["single"].replace(B=3, S=S, Hq=Hq, Hkv=Hkv, qkv_scale=1.0)
     cache, q, kb, vb = support.attention_case(cfg, seed=S + Hq, lens=[0, 700, 1500])
     _check(cfg, cache, q, kb, vb)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_single_query_decode_shape(dtype):
+    """S = 1 (one query per head, the autoregressive decode shape) on the same paged cache:
+    the CUDA-core kernel, ragged lengths including 0, against the oracle."""
+    base = synth.CONFIGS["single"] if dtype == "bf16" else synth.CONFIGS["tiny"]
+    cfg = base.replace(B=4, S=1, qkv_scale=1.0)
+    lens = [0, 1, 777, 4096] if dtype == "bf16" else [0, 1, 37, 64]
+    _check(cfg, *support.attention_case(cfg, seed=31, lens=lens))

@@ -58,10 +58,12 @@ def test_single_bf16_full_vocab(peak_hi):
         _check_step(lg, "bf16", masked, tokens, cfg.tau, step, cfg.T)
 
 
-def test_batch_sharp_variant_every_branch():
+@pytest.mark.parametrize("tau", [0.9, 0.8])
+def test_batch_sharp_variant_every_branch(tau):
     """B=32, V=131072; peaks U[0,40] in half the sequences and U[0,12] in the other half, so that
-    the threshold, the fallback and step T all occur."""
-    cfg = synth.CONFIGS["ctx8k"]
+    the threshold, the fallback and step T all occur; at the workloads' threshold 0.9 and at the
+    0.8 one of the pages' two-GPU runs."""
+    cfg = synth.CONFIGS["ctx8k"].replace(tau=tau)
     rng = np.random.default_rng(11)
     ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.bfloat16))
     lg = synth.draw_logits(cfg, seed=5, peak_hi=40.0)
