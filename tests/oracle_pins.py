@@ -211,6 +211,28 @@ def check_attention_invariants(impl, seed=3):
     assert np.array_equal(o5, o)
 
 
+def check_attention_segment_merge(impl, seed=14):
+    """Attention over [context ; block] is the log-sum-exp weighted merge of attention over
+    each segment alone (the block removed with -inf scores, or no context):
+    lse = logaddexp(lse_c, lse_b) and o = (e^lse_c o_c + e^lse_b o_b) / e^lse."""
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D, L = 4, 6, 2, 5, 19
+    q = rng.normal(size=(S, Hq, D)) * 1.5
+    kc, vc = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+    kb, vb = rng.normal(size=(S, Hkv, D)), rng.normal(size=(S, Hkv, D))
+    o, lse = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.8)
+    bias = np.zeros(L + S)
+    bias[L:] = -np.inf
+    o_c, lse_c = impl.denoise_attention_seq(q, kc, vc, kb, vb, 0.8, key_bias=bias)
+    empty = np.zeros((0, Hkv, D))
+    o_b, lse_b = impl.denoise_attention_seq(q, empty, empty, kb, vb, 0.8)
+    want_lse = np.logaddexp(lse_c, lse_b)                      # [Hq, S]
+    assert np.allclose(lse, want_lse, rtol=0, atol=1e-12)
+    w_c = np.exp(lse_c - want_lse).T[:, :, None]               # [S, Hq, 1]
+    w_b = np.exp(lse_b - want_lse).T[:, :, None]
+    assert np.allclose(o, w_c * o_c + w_b * o_b, rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------------------------ causal-block attention pins
 # The context tower taking in a committed block: block query i sees every context key and
 # the block keys 0..i (gist.science summary, "Technisches Resümee — Architektur": the frozen
@@ -588,7 +610,7 @@ def check_masked_nll_invariants(impl, seed=13):
 
 
 ALL_CHECKS = [check_attention_bruteforce, check_attention_sdpa, check_attention_closed_forms,
-              check_attention_invariants, check_causal_block_bruteforce, check_causal_block_sdpa,
+              check_attention_invariants, check_attention_segment_merge, check_causal_block_bruteforce, check_causal_block_sdpa,
               check_causal_block_closed_forms, check_causal_block_invariants, check_unmask_closed_forms, check_unmask_bruteforce,
               check_unmask_rules, check_block_loop, check_append, check_linear_schedule,
               check_masked_nll_closed_forms, check_masked_nll_library, check_masked_nll_invariants]

@@ -21,21 +21,22 @@ pytestmark = pytest.mark.gpu
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
-def _run(cfg, cache_h, q, kb, vb, max_ctas=0, ws=None, check_err=True):
+def _run(cfg, cache_h, q, kb, vb, max_ctas=0, ws=None, check_err=True, scale=None):
     cache = support.cache_to_dev(cache_h)
     qd, kd, vd = (support.to_dev(x, cfg.dtype) for x in (q, kb, vb))
     lse = torch.full((cfg.B, cfg.Hq, cfg.S), float("nan"), device="cuda")
     err = api.error_word()
-    out = api.tt_denoise_attn(cache, qd, kd, vd, lse=lse, sm_scale=1.0 / math.sqrt(cfg.D), max_ctas=max_ctas,
-                              ws=ws, dev_err=err)
+    scale = 1.0 / math.sqrt(cfg.D) if scale is None else scale
+    out = api.tt_denoise_attn(cache, qd, kd, vd, lse=lse, sm_scale=scale, max_ctas=max_ctas, ws=ws, dev_err=err)
     code = api.tt_get_device_error(err)
     if check_err:
         assert code == 0, code
     return support.to_host_f64(out, cfg.dtype), lse.cpu().numpy().astype(np.float64), code, out
 
 
-def _oracle_groups(cfg, cache_h, q, kb, vb, pairs):
+def _oracle_groups(cfg, cache_h, q, kb, vb, pairs, scale=None):
     """Oracle output of selected (sequence, KV head) pairs: dict (b, g) -> (o [S,G,D], lse [G,S])."""
+    scale = 1.0 / math.sqrt(cfg.D) if scale is None else scale
     res = {}
     for b, g in pairs:
         L = int(cache_h.ctx_len[b])
@@ -45,15 +46,15 @@ def _oracle_groups(cfg, cache_h, q, kb, vb, pairs):
         res[(b, g)] = oracle.denoise_attention_seq(
             oracle.decode(q[b][:, hs], cfg.dtype), kc[:, g:g + 1], vc[:, g:g + 1],
             oracle.decode(kb[b][:, g:g + 1], cfg.dtype), oracle.decode(vb[b][:, g:g + 1], cfg.dtype),
-            1.0 / math.sqrt(cfg.D))
+            scale)
     return res
 
 
-def _check(cfg, cache_h, q, kb, vb, pairs=None, max_ctas=0, tol=None):
-    o, lse, _, _ = _run(cfg, cache_h, q, kb, vb, max_ctas=max_ctas)
+def _check(cfg, cache_h, q, kb, vb, pairs=None, max_ctas=0, tol=None, scale=None):
+    o, lse, _, _ = _run(cfg, cache_h, q, kb, vb, max_ctas=max_ctas, scale=scale)
     if pairs is None:
         pairs = [(b, g) for b in range(cfg.B) for g in range(cfg.Hkv)]
-    want = _oracle_groups(cfg, cache_h, q, kb, vb, pairs)
+    want = _oracle_groups(cfg, cache_h, q, kb, vb, pairs, scale=scale)
     tol = TOL[cfg.dtype] if tol is None else tol
     worst = 0.0
     for (b, g), (wo, wl) in want.items():
@@ -219,3 +220,12 @@ def test_single_query_decode_shape(dtype):
     cfg = base.replace(B=4, S=1, qkv_scale=1.0)
     lens = [0, 1, 777, 4096] if dtype == "bf16" else [0, 1, 37, 64]
     _check(cfg, *support.attention_case(cfg, seed=31, lens=lens))
+
+
+@pytest.mark.parametrize("name,scale", [("single", 0.3), ("single", 0.02), ("tiny", 0.5), ("single", -0.05)])
+def test_softmax_scale_argument(name, scale):
+    """Scales other than 1/sqrt(D): sharper and flatter weights on the tensor-core kernel, the
+    fp32 kernel, and a negative scale (taken by the CUDA-core kernel), with the LSE."""
+    cfg = synth.CONFIGS[name].replace(B=2, qkv_scale=1.0)
+    lens = [cfg.len_lo, 130] if name == "single" else [64, 5]
+    _check(cfg, *support.attention_case(cfg, seed=33, lens=lens), scale=scale)
