@@ -241,6 +241,7 @@ def test_unmutated_copy_passes():
         check(impl)
 
 
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")   # overflow / NaN is how some mistakes show
 @pytest.mark.parametrize("name,override", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(name, override):
     impl = _impl(**override)
