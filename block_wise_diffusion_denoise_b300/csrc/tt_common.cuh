@@ -29,7 +29,10 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
     return u >> 16;
 }
 
-// 2^x on the special-function unit (x <= 0 here; flushes denormal results to zero).
+// 2^x on the special-function unit (flushes denormal results to zero).  Callers pass
+// exponents up to +8 as well: the attention's lazy rescale lets a tile's scores exceed
+// the running maximum by up to 2^8 before it moves, so P <= 2^8 (exact enough in bf16,
+// and far from overflow in the fp32 sums).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

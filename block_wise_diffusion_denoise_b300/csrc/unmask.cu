@@ -728,9 +728,23 @@ static __device__ __align__(256) unsigned char g_unmask_scratch[TT_UNMASK_NOALLO
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_scratch_once[kMaxDevices];
-void *g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices];   // set only by a lookup that succeeded
+
+// Device address of the scratch array on device `dev` (current), looked up on the first
+// call that succeeds; a failed lookup is not remembered, so a later call tries again.
+void *scratch_address(int dev) {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_unmask_scratch) != cudaSuccess) {
+            cudaGetLastError();   // take back the error it recorded, so no later check sees it
+            return nullptr;
+        }
+        g_scratch_ptr[dev] = ptr;
+    }
+    return g_scratch_ptr[dev];
+}
 
 }  // namespace
 
@@ -745,11 +759,8 @@ tt_status launch_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S
     if (dev < 0 || dev >= kMaxDevices) return TT_ERR_UNSUPPORTED;
     // Host code only holds a stand-in for the array; its device address comes from
     // the runtime, once per device, with that device current.
-    std::call_once(g_scratch_once[dev], [dev] {
-        g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_unmask_scratch);
-    });
-    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) return TT_ERR_CUDA;
-    void *ws = g_scratch_ptr[dev];
+    void *ws = scratch_address(dev);
+    if (ws == nullptr) return TT_ERR_CUDA;
     // The per-sequence counters must start at zero, whatever an earlier call left.
     const size_t tick_off = unmask_tickets_off(B, S, V, dtype);
     if (cudaMemsetAsync(static_cast<char *>(ws) + tick_off, 0, (size_t)B * sizeof(unsigned), stream) !=

@@ -35,7 +35,11 @@
  *     tt_get_device_error synchronises.
  *   - Every pointer argument marked "device" is device memory owned by the
  *     caller.  The library never allocates or frees memory and keeps no state
- *     between calls; it is safe to call from several host threads.
+ *     between calls; it is safe to call from several host threads.  The one
+ *     exception is tt_unmask_noalloc: it keeps its scratch in a device array of
+ *     the library's own (shared by all its calls, which therefore must not
+ *     overlap on the GPU) and caches that array's address per device; its own
+ *     comment below gives the rules.
  *   - Workspace: each call that needs scratch takes (ws, ws_bytes); the size
  *     comes from the matching *_workspace_size function.  The workspace must be
  *     zero-filled before its first use; the kernels leave their counters at zero
@@ -226,7 +230,8 @@ TT_API tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int
  *
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
- *    capture.
+ *    capture.  If that lookup fails the call returns TT_ERR_CUDA and the next
+ *    call on the device tries again (nothing is latched on failure).
  *  - A shape whose scratch would exceed the array returns TT_ERR_CAPACITY before
  *    anything is launched (tt_unmask_workspace_size gives the need; about 82 KB
  *    for 32 sequences x 16 positions x 131072 bf16 logits).

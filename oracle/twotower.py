@@ -210,6 +210,26 @@ def unmask_seq(logits: np.ndarray, masked: np.ndarray, tokens: np.ndarray, tau: 
         z = np.exp(row - m).sum()
         conf[p] = 1.0 / z
         arg[p] = int(np.argmax(row))            # first index of the maximum
+    committed, fallback = commit_rule(conf, masked, tau, step, T)
+    new_tokens = np.array(tokens, dtype=np.int64, copy=True)
+    new_masked = masked.copy()
+    for p in np.nonzero(committed)[0]:
+        new_tokens[p] = arg[p]
+        new_masked[p] = False
+    return UnmaskResult(new_tokens, new_masked, committed, conf, arg, fallback)
+
+
+def commit_rule(conf: np.ndarray, masked: np.ndarray, tau: float, step: int, T: int):
+    """Which masked positions the step commits, given their confidences ([U]).
+
+    C = {p masked : conf_p >= tau}; at step T (step >= T) C is every masked
+    position; otherwise, if C is empty and a position is still masked, C holds
+    the single most confident masked position (the lowest p on ties).  Only the
+    entries of ``conf`` at masked positions are read.  Returns (committed [S]
+    bool, fallback) where ``fallback`` says the at-least-one rule made the choice.
+    """
+    S = len(masked)
+    masked = np.asarray(masked, dtype=bool)
     cand = [p for p in range(S) if masked[p]]
     chosen = [p for p in cand if conf[p] >= tau]
     fallback = False
@@ -222,14 +242,9 @@ def unmask_seq(logits: np.ndarray, masked: np.ndarray, tokens: np.ndarray, tau: 
                 best = p
         chosen = [best]
         fallback = True
-    new_tokens = np.array(tokens, dtype=np.int64, copy=True)
-    new_masked = masked.copy()
     committed = np.zeros(S, dtype=bool)
-    for p in chosen:
-        new_tokens[p] = arg[p]
-        new_masked[p] = False
-        committed[p] = True
-    return UnmaskResult(new_tokens, new_masked, committed, conf, arg, fallback)
+    committed[chosen] = True
+    return committed, fallback
 
 
 def unmask(logits: np.ndarray, masked: np.ndarray, tokens: np.ndarray, tau: float, step: int,

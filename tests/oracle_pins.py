@@ -1,9 +1,10 @@
 """Checks that pin the float64 oracle to things other than itself.
 
 Each ``check_*`` takes an implementation namespace ``impl`` exposing
-``context_rows``, ``denoise_attention_seq``, ``unmask_seq``, ``kv_append``,
-``linear_schedule_mask`` and ``masked_nll_seq`` (the oracle, or a deliberately
-broken copy of it) and raises AssertionError if the implementation disagrees
+``decode``, ``context_rows``, ``denoise_attention_seq``, ``denoise_attention``,
+``unmask_seq``, ``commit_rule``, ``unmask``, ``kv_append``, ``linear_schedule_mask``,
+``masked_nll_seq`` and ``masked_nll`` (the oracle, or a deliberately broken copy
+of it) and raises AssertionError if the implementation disagrees
 with:
 
 * brute force (pure-Python loops, a different route to the same definition),
@@ -609,8 +610,132 @@ def check_masked_nll_invariants(impl, seed=13):
         assert math.isclose(nll[p], want, rel_tol=0, abs_tol=1e-12)
 
 
+# ------------------------------------------------------------------ decoding and the batched wrappers
+
+def _torch_decode_bf16(bits):
+    """bf16 bit patterns -> float64 through PyTorch's own bfloat16 conversion (no oracle code)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.double().numpy()
+
+
+def check_decode(impl, seed=15):
+    """Every one of the 65536 bf16 bit patterns decodes to the value PyTorch gives it (NaN
+    patterns to NaN), and float32 storage decodes to its exact float64 value."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):          # signalling-NaN patterns widen with a warning
+        got = impl.decode(bits, "bf16")
+    want = _torch_decode_bf16(bits)
+    nan = np.isnan(want)
+    assert nan.sum() == 254                       # 2 signs x 127 non-zero mantissas at exponent 255
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))   # -0.0 stays negative
+    # a few values written out from the bfloat16 format: sign, 8 exponent bits, 7 mantissa bits
+    spot = {0x3F80: 1.0, 0xBF80: -1.0, 0x4049: 3.140625, 0x0001: 2.0 ** -133, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127,
+            0x7F80: math.inf, 0xFF80: -math.inf, 0x3C00: 2.0 ** -7, 0xC2F7: -123.5}
+    for b, v in spot.items():
+        assert impl.decode(np.array([b], np.uint16), "bf16")[0] == v, hex(b)
+    # shape is kept
+    with np.errstate(invalid="ignore"):
+        assert impl.decode(bits.reshape(256, 256), "bf16").shape == (256, 256)
+    # float32 storage: exact widening, specials included
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(1000).astype(np.float32) * np.float32(1e3)
+    x[:6] = [0.0, -0.0, np.inf, -np.inf, np.float32(1e-45), np.float32(3.4e38)]
+    got = impl.decode(x, "f32")
+    assert got.dtype == np.float64
+    assert np.array_equal(got, torch.from_numpy(x).double().numpy())
+    assert np.signbit(got[1])
+
+
+def check_commit_rule(impl):
+    """The commit rule on confidences written out by hand."""
+    nan = float("nan")
+    cases = [
+        # conf, masked, tau, step, T -> committed, fallback
+        ([0.95, 0.2, 0.9, 0.5], [1, 1, 1, 1], 0.9, 1, 4, [1, 0, 1, 0], False),   # >= tau, tau itself commits
+        ([0.3, 0.7, 0.7, 0.1], [1, 1, 1, 1], 0.9, 2, 4, [0, 1, 0, 0], True),     # fallback, tie -> lowest p
+        ([0.3, 0.7, 0.8, 0.1], [1, 1, 1, 1], 0.9, 2, 4, [0, 0, 1, 0], True),     # fallback, most confident
+        ([0.3, nan, 0.2, 0.1], [1, 0, 1, 1], 0.9, 3, 4, [1, 0, 0, 0], True),     # locked entries not read
+        ([0.3, nan, 0.2, 0.1], [1, 0, 1, 1], 0.9, 4, 4, [1, 0, 1, 1], False),    # step T: all masked
+        ([0.3, nan, 0.2, 0.1], [1, 0, 1, 1], 0.9, 7, 4, [1, 0, 1, 1], False),    # past T as well
+        ([0.99, 0.99, 0.99], [0, 0, 0], 0.9, 1, 4, [0, 0, 0], False),            # nothing masked
+        ([0.99, 0.95, 0.2], [0, 1, 1], 0.9, 1, 4, [0, 1, 0], False),             # locked confident row ignored
+        ([0.5], [1], 0.5, 1, 4, [1], False),                                     # exactly tau
+        ([0.5], [1], 0.5000001, 1, 4, [1], True),                                # just above: fallback
+    ]
+    for conf, masked, tau, step, T, want, fb in cases:
+        com, fallback = impl.commit_rule(np.array(conf), np.array(masked, bool), tau, step, T)
+        assert [int(c) for c in com] == want, (conf, masked, tau, step, T)
+        assert bool(fallback) == fb, (conf, masked, tau, step, T)
+
+
+def _walk_pages(pool, table_row, L, page_size):
+    """The first L context rows of a sequence by an explicit loop over positions."""
+    rows = []
+    for j in range(L):
+        rows.append(pool[int(table_row[j // page_size]), :, j % page_size, :])
+    return np.stack(rows) if rows else np.zeros((0, pool.shape[1], pool.shape[3]), pool.dtype)
+
+
+def check_batched_wrappers(impl, seed=16):
+    """The batched entry points equal a loop over the per-sequence functions on a ragged
+    three-sequence batch: pages walked position by position, values decoded by PyTorch,
+    locked rows given as NaN (they must not be read), and the ``seqs`` selection honoured."""
+    rng = np.random.default_rng(seed)
+    B, S, Hq, Hkv, D, page, V = 3, 4, 4, 2, 8, 4, 50
+    lens = np.array([5, 0, 11])
+    maxp = 3
+    num_pages = B * maxp + 2
+    table = rng.permutation(num_pages)[:B * maxp].reshape(B, maxp)
+    f32 = lambda shape: rng.standard_normal(shape).astype(np.float32)   # noqa: E731
+    bits = lambda x: (x.view(np.uint32) >> 16).astype(np.uint16)         # noqa: E731  (truncation: exact bf16 values)
+    kp, vp = bits(f32((num_pages, Hkv, page, D))), bits(f32((num_pages, Hkv, page, D)))
+    q, kb, vb = bits(f32((B, S, Hq, D))), bits(f32((B, S, Hkv, D))), bits(f32((B, S, Hkv, D)))
+    dec = _torch_decode_bf16
+    o, lse = impl.denoise_attention(kp, vp, table, lens, page, q, kb, vb, 0.3, "bf16")
+    for b in range(B):
+        kc = dec(_walk_pages(kp, table[b], int(lens[b]), page))
+        vc = dec(_walk_pages(vp, table[b], int(lens[b]), page))
+        wo, wl = impl.denoise_attention_seq(dec(q[b]), kc, vc, dec(kb[b]), dec(vb[b]), 0.3)
+        assert np.array_equal(o[b], wo) and np.array_equal(lse[b], wl), b
+    o2, lse2 = impl.denoise_attention(kp, vp, table, lens, page, q, kb, vb, 0.3, "bf16", seqs=[2])
+    assert np.isnan(o2[:2]).all() and np.isnan(lse2[:2]).all() and np.array_equal(o2[2], o[2])
+    # unmasking: locked rows are passed as NaN to the per-sequence rule
+    lg = bits(f32((B, S, V)) * np.float32(3))
+    masked = np.array([[1, 0, 1, 1], [0, 0, 0, 0], [1, 1, 0, 1]], np.uint8)
+    tokens = np.where(masked == 1, -1, 7 + np.arange(B * S).reshape(B, S))
+    res = impl.unmask(lg, masked, tokens, 0.9, 2, 4, "bf16")
+    for b in range(B):
+        rows = np.full((S, V), np.nan)
+        for p in range(S):
+            if masked[b, p]:
+                rows[p] = dec(lg[b, p])
+        want = impl.unmask_seq(rows, masked[b].astype(bool), tokens[b], 0.9, 2, 4)
+        got = res[b]
+        assert np.array_equal(got.tokens, want.tokens) and np.array_equal(got.masked, want.masked), b
+        assert np.array_equal(got.committed_now, want.committed_now) and got.fallback == want.fallback, b
+        assert np.array_equal(got.conf, want.conf, equal_nan=True) and np.array_equal(got.argmax, want.argmax), b
+    res = impl.unmask(lg, masked, tokens, 0.9, 2, 4, "bf16", seqs=[0, 2])
+    assert res[1] is None and res[0] is not None and res[2] is not None
+    # masked NLL: same marshalling
+    tg = rng.integers(0, V, size=(B, S))
+    nll, sums, counts = impl.masked_nll(lg, tg, masked, "bf16")
+    for b in range(B):
+        rows = np.full((S, V), np.nan)
+        for p in range(S):
+            if masked[b, p]:
+                rows[p] = dec(lg[b, p])
+        wn, wt, wc = impl.masked_nll_seq(rows, tg[b], masked[b].astype(bool))
+        assert np.array_equal(nll[b], wn, equal_nan=True) and sums[b] == wt and counts[b] == wc, b
+    nll2, sums2, counts2 = impl.masked_nll(lg, tg, masked, "bf16", seqs=[1])
+    assert np.isnan(nll2[[0, 2]]).all() and np.isnan(sums2[[0, 2]]).all() and (counts2[[0, 2]] == -1).all()
+    assert counts2[1] == 0 and sums2[1] == 0.0
+
+
 ALL_CHECKS = [check_attention_bruteforce, check_attention_sdpa, check_attention_closed_forms,
               check_attention_invariants, check_attention_segment_merge, check_causal_block_bruteforce, check_causal_block_sdpa,
               check_causal_block_closed_forms, check_causal_block_invariants, check_unmask_closed_forms, check_unmask_bruteforce,
               check_unmask_rules, check_block_loop, check_append, check_linear_schedule,
-              check_masked_nll_closed_forms, check_masked_nll_library, check_masked_nll_invariants]
+              check_masked_nll_closed_forms, check_masked_nll_library, check_masked_nll_invariants,
+              check_decode, check_commit_rule, check_batched_wrappers]

@@ -16,7 +16,7 @@ from tests import support
 pytestmark = pytest.mark.gpu
 
 
-def _run_loop(cfg, lens, seed, peak_hi, sample=None):
+def _run_loop(cfg, lens, seed, peak_hi, sample=None, name="block loop"):
     """Runs the loop; checks everything against the oracle, or with ``sample`` (a function of
     (block, step) returning ([(layer, sequence), ...] for attention, [sequence, ...] for the
     unmasking)) only those, plus the rules' oracle-free checks on every sequence."""
@@ -34,6 +34,7 @@ def _run_loop(cfg, lens, seed, peak_hi, sample=None):
     ws = api.workspace(api.tt_block_step_workspace_size(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.D, cfg.V, tdt))
     err = api.error_word()
     steps_run = 0
+    stats = support.UnmaskStats()
     for blk in range(cfg.n_blocks):
         masked = torch.ones((cfg.B, cfg.S), dtype=torch.uint8, device="cuda")
         tokens = torch.full((cfg.B, cfg.S), -1, dtype=torch.int32, device="cuda")
@@ -69,9 +70,9 @@ def _run_loop(cfg, lens, seed, peak_hi, sample=None):
                     assert support.max_abs(got[b], want[b]) <= tol, (blk, step, l, b)
             # the unmasking against the oracle from the GPU's pre-step state
             ora = oracle.unmask(lg, pre_m, pre_t, cfg.tau, step, cfg.T, cfg.dtype, seqs=unmask_seqs)
-            support.compare_unmask(pre_m, pre_t, ora, masked.cpu().numpy(), tokens.cpu().numpy(),
-                                   com.cpu().numpy(), conf.cpu().numpy(), nm.cpu().numpy(), cfg.tau, step,
-                                   cfg.T)
+            stats += support.compare_unmask(pre_m, pre_t, ora, masked.cpu().numpy(), tokens.cpu().numpy(),
+                                            com.cpu().numpy(), conf.cpu().numpy(), nm.cpu().numpy(), cfg.tau,
+                                            step, cfg.T)
             steps_run += 1
             if not masked.any():
                 break
@@ -86,6 +87,8 @@ def _run_loop(cfg, lens, seed, peak_hi, sample=None):
                                        cfg.page_size)
         ctx = new_ctx
         assert np.array_equal(devs[0].ctx_len.cpu().numpy(), ctx)
+    support.report(name, stats)
+    stats.check_bounds()
     return steps_run
 
 
@@ -95,7 +98,7 @@ def test_block_loop_bf16_in_lockstep(peak_hi):
     ragged context, 3 attention layers, T=4, 3 blocks, V=8192."""
     cfg = synth.CONFIGS["loop"].replace(B=3, n_layers=3, T=4, n_blocks=3, V=8192, len_lo=100, len_hi=700)
     lens = np.array([100, 420, 700], np.int32)
-    assert _run_loop(cfg, lens, seed=3, peak_hi=peak_hi) >= cfg.n_blocks
+    assert _run_loop(cfg, lens, seed=3, peak_hi=peak_hi, name=f"block loop bf16 peak {peak_hi}") >= cfg.n_blocks
 
 
 def test_full_size_block_loop_sampled():
@@ -111,10 +114,10 @@ def test_full_size_block_loop_sampled():
         i = blk * cfg.T + step
         return [(i % cfg.n_layers, (7 * i) % cfg.B)], sorted({(5 * i) % cfg.B, (5 * i + 3) % cfg.B})
 
-    assert _run_loop(cfg, lens, seed=11, peak_hi=12.0, sample=sample) >= cfg.n_blocks
+    assert _run_loop(cfg, lens, seed=11, peak_hi=12.0, sample=sample, name="block loop full size") >= cfg.n_blocks
 
 
 def test_block_loop_fp32_in_lockstep():
     cfg = synth.CONFIGS["tiny"].replace(B=2, n_layers=2, n_blocks=2, T=4)
     lens = np.array([64, 5], np.int32)
-    assert _run_loop(cfg, lens, seed=4, peak_hi=None) >= cfg.n_blocks
+    assert _run_loop(cfg, lens, seed=4, peak_hi=None, name="block loop fp32") >= cfg.n_blocks

@@ -201,12 +201,120 @@ def _nll_mutant(kind):
     return nll_seq
 
 
+def _decode_mutant(kind):
+    def decode(x, dtype):
+        if dtype == "bf16":
+            if kind == "sign_extend":            # the 16-bit pattern taken as a signed integer
+                bits = np.asarray(x).astype(np.uint16).view(np.int16).astype(np.int32) >> 0
+                bits = (bits.astype(np.int64) << 16).astype(np.uint32) | \
+                    (np.uint32(0xFFFF) * (bits < 0)).astype(np.uint32)   # ones smeared into the low half
+                return bits.view(np.float32).astype(np.float64)
+            shift = 15 if kind == "shift_15" else 16
+            bits = np.asarray(x).astype(np.uint32) << np.uint32(shift)
+            if kind == "low_half":               # the pattern read as the low half of a float32
+                bits = np.asarray(x).astype(np.uint32)
+            return bits.view(np.float32).astype(np.float64)
+        if kind == "f32_via_bf16":               # float32 storage truncated to bf16 precision
+            u = np.asarray(x, dtype=np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+            return u.view(np.float32).astype(np.float64)
+        return np.asarray(x, dtype=np.float32).astype(np.float64)
+    return decode
+
+
+def _commit_rule_mutant(kind):
+    def rule(conf, masked, tau, step, T):
+        S = len(masked)
+        masked = np.asarray(masked, dtype=bool)
+        cand = [p for p in range(S) if masked[p]]
+        if kind == "strict":
+            chosen = [p for p in cand if conf[p] > tau]
+        elif kind == "reads_locked":
+            chosen = [p for p in range(S) if conf[p] >= tau]
+        else:
+            chosen = [p for p in cand if conf[p] >= tau]
+        fallback = False
+        if step >= T and kind != "no_step_T":
+            chosen = cand
+        elif not chosen and cand:
+            best = cand[0]
+            for p in cand[1:]:
+                if (conf[p] >= conf[best]) if kind == "tie_last" else (conf[p] > conf[best]):
+                    best = p
+            chosen = [best]
+            fallback = True
+        committed = np.zeros(S, dtype=bool)
+        committed[chosen] = True
+        return committed, fallback
+    return rule
+
+
+def _batched_attention_mutant(kind):
+    def denoise_attention(k_pool, v_pool, page_table, ctx_len, page_size, q, k_blk, v_blk, sm_scale, dtype,
+                          seqs=None, causal_block=False):
+        B, S, Hq, D = q.shape
+        o = np.full((B, S, Hq, D), np.nan)
+        lse = np.full((B, Hq, S), np.nan)
+        for b in (range(B) if seqs is None or kind == "ignore_seqs" else seqs):
+            L = int(ctx_len[b])
+            tb = page_table[(b + 1) % B] if kind == "next_table" else page_table[b]
+            if kind == "len_minus_one":
+                L = max(0, L - 1)
+            kc = oracle.decode(oracle.context_rows(k_pool, tb, L, page_size), dtype)
+            vc = oracle.decode(oracle.context_rows((k_pool if kind == "k_pool_twice" else v_pool), tb, L,
+                                                   page_size), dtype)
+            o[b], lse[b] = oracle.denoise_attention_seq(oracle.decode(q[b], dtype), kc, vc,
+                                                        oracle.decode(k_blk[b], dtype),
+                                                        oracle.decode(v_blk[b], dtype), sm_scale,
+                                                        causal_block=causal_block)
+        return o, lse
+    return denoise_attention
+
+
+def _batched_unmask_mutant(kind):
+    def unmask(logits, masked, tokens, tau, step, T, dtype, seqs=None):
+        B = logits.shape[0]
+        res = []
+        for b in range(B):
+            if seqs is not None and b not in seqs and kind != "ignore_seqs":
+                res.append(None)
+                continue
+            lg = np.full((logits.shape[1], logits.shape[2]), np.nan)
+            for p in range(logits.shape[1]):
+                if masked[b, p]:
+                    lg[p] = oracle.decode(logits[(b + 1) % B if kind == "next_row" else b, p], dtype)
+            res.append(oracle.unmask_seq(lg, masked[b], tokens[0] if kind == "first_tokens" else tokens[b],
+                                         tau, step, T))
+        return res
+    return unmask
+
+
+def _batched_nll_mutant(kind):
+    def masked_nll(logits, targets, masked, dtype, seqs=None):
+        B, S = masked.shape
+        nll = np.full((B, S), np.nan)
+        sums = np.full(B, np.nan)
+        counts = np.full(B, -1, dtype=np.int64)
+        for b in (range(B) if seqs is None else seqs):
+            lg = np.full((S, logits.shape[2]), np.nan)
+            for p in range(S):
+                if masked[b, p]:
+                    lg[p] = oracle.decode(logits[b, p], dtype)
+            tg = targets[b][::-1] if kind == "targets_reversed" else targets[b]
+            nll[b], sums[b], counts[b] = oracle.masked_nll_seq(lg, tg, masked[b])
+            if kind == "mean_not_sum" and counts[b] > 0:
+                sums[b] /= counts[b]
+        return nll, sums, counts
+    return masked_nll
+
+
 def _impl(**override):
-    ns = types.SimpleNamespace(context_rows=oracle.context_rows,
+    ns = types.SimpleNamespace(decode=oracle.decode, context_rows=oracle.context_rows,
                                denoise_attention_seq=oracle.denoise_attention_seq,
-                               unmask_seq=oracle.unmask_seq, kv_append=oracle.kv_append,
+                               denoise_attention=oracle.denoise_attention,
+                               unmask_seq=oracle.unmask_seq, commit_rule=oracle.commit_rule,
+                               unmask=oracle.unmask, kv_append=oracle.kv_append,
                                linear_schedule_mask=oracle.linear_schedule_mask,
-                               masked_nll_seq=oracle.masked_nll_seq)
+                               masked_nll_seq=oracle.masked_nll_seq, masked_nll=oracle.masked_nll)
     for k, v in override.items():
         setattr(ns, k, v)
     return ns
@@ -229,6 +337,16 @@ MUTANTS = (
     + [("nll_" + k, dict(masked_nll_seq=_nll_mutant(k)))
        for k in ("include_unmasked", "no_max_shift", "target_off_by_one", "wrong_sign", "max_not_lse",
                  "count_all")]
+    + [("decode_" + k, dict(decode=_decode_mutant(k)))
+       for k in ("sign_extend", "shift_15", "low_half", "f32_via_bf16")]
+    + [("rule_" + k, dict(commit_rule=_commit_rule_mutant(k)))
+       for k in ("strict", "reads_locked", "tie_last", "no_step_T")]
+    + [("batched_attn_" + k, dict(denoise_attention=_batched_attention_mutant(k)))
+       for k in ("ignore_seqs", "next_table", "len_minus_one", "k_pool_twice")]
+    + [("batched_unmask_" + k, dict(unmask=_batched_unmask_mutant(k)))
+       for k in ("ignore_seqs", "first_tokens", "next_row")]
+    + [("batched_nll_" + k, dict(masked_nll=_batched_nll_mutant(k)))
+       for k in ("targets_reversed", "mean_not_sum")]
 )
 
 
@@ -236,7 +354,9 @@ def test_unmutated_copy_passes():
     impl = _impl(denoise_attention_seq=_attention_mutant("none"),
                  context_rows=_context_rows_mutant("none"), unmask_seq=_unmask_mutant("none"),
                  kv_append=_append_mutant("none"), linear_schedule_mask=_schedule_mutant("none"),
-                 masked_nll_seq=_nll_mutant("none"))
+                 masked_nll_seq=_nll_mutant("none"), decode=_decode_mutant("none"),
+                 commit_rule=_commit_rule_mutant("none"), denoise_attention=_batched_attention_mutant("none"),
+                 unmask=_batched_unmask_mutant("none"), masked_nll=_batched_nll_mutant("none"))
     for check in oracle_pins.ALL_CHECKS:
         check(impl)
 

@@ -46,9 +46,14 @@ def _outputs(cfg, dtype, lg_dev, masked, tokens, step, noalloc):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,dtype", [("ctx8k", "bf16"), ("tiny", "f32")])
+@pytest.mark.parametrize("name,dtype", [("ctx8k", "bf16"), ("tiny", "f32"), ("large_batch", "f32")])
 def test_noalloc_matches_workspace_entry_point_twice(name, dtype):
-    cfg = synth.CONFIGS[name].replace(dtype=dtype)
+    """ctx8k takes the streaming kernel at full vocabulary; large_batch (260 sequences x 16
+    positions, above the streaming kernel's 4096-row list, V = 1024) takes the chunked one."""
+    if name == "large_batch":
+        cfg = synth.CONFIGS["single"].replace(B=260, V=1024, dtype=dtype)
+    else:
+        cfg = synth.CONFIGS[name].replace(dtype=dtype)
     lg = synth.draw_logits(cfg, seed=21, peak_hi=40.0)
     if cfg.B > 1:
         lg[cfg.B // 2:] = synth.draw_logits(cfg, seed=22, peak_hi=12.0)[cfg.B // 2:]
