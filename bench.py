@@ -56,7 +56,8 @@ def parse():
 CSRC = os.path.join(ROOT, "block_wise_diffusion_denoise_b300", "csrc")
 PROFILED = {   # kernel -> (summary under profiles/, the sources its counters were taken from)
     "attention": ("attention_ctx8k.md", ("attn_tc.cu", "sm100_ptx.cuh", "tt_common.cuh")),
-    "unmask": ("unmask_ctx8k.md", ("unmask.cu", "sm100_ptx.cuh", "tt_common.cuh")),
+    "unmask": ("unmask_ctx8k.md", ("unmask.cu", "vocab_stream.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
+    "masked_nll": ("masked_nll_ctx8k.md", ("masked_nll.cu", "vocab_stream.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
 }
 
 
@@ -387,6 +388,20 @@ def run_ours(a, cfg):
         api.tt_unmask(c["lg"], unm_masked[i], unm_tokens[i], cfg.tau, 1, cfg.T, ws=unm_ws, dev_err=err,
                       stream=stream)
 
+    # the masked-diffusion loss over the same logits, every position masked (the unmasking's
+    # bytes: masked rows x V)
+    nll_ws = api.workspace(api.tt_masked_nll_workspace_size(cfg.B, cfg.S, cfg.V, tdt), dev)
+    nll_targets = torch.from_numpy(synth.draw_corruption(cfg, seed)[0]).to(dev)
+    nll_masked = torch.ones((cfg.B, cfg.S), dtype=torch.uint8, device=dev)
+    nll_out = torch.empty((cfg.B, cfg.S), dtype=torch.float32, device=dev)
+    nll_sum = torch.empty((cfg.B,), dtype=torch.float32, device=dev)
+    nll_cnt = torch.empty((cfg.B,), dtype=torch.int32, device=dev)
+
+    def nll_only(i, stream=None):
+        c = copies[i % n_copies]
+        api.tt_masked_nll(c["lg"], nll_targets, nll_masked, nll=nll_out, nll_sum=nll_sum, count=nll_cnt, ws=nll_ws,
+                          dev_err=err, stream=stream)
+
     def barrier():
         if world > 1:
             dist.barrier()
@@ -466,6 +481,8 @@ def run_ours(a, cfg):
     unmask_ms = timed(unmask_only, 0, k_ker, use_graph) / k_ker
     # the context tower's causal view of the same block (not part of the denoise step)
     ctx_attn_ms = timed(ctx_attn_only, 0, k_ker, use_graph) / k_ker
+    # the training-side loss over the same logits (not part of the denoise step)
+    nll_ms = timed(nll_only, 0, k_ker, use_graph) / k_ker
     if api.tt_get_device_error(err) != 0:
         raise SystemExit("device error in the per-kernel timings")
 
@@ -565,6 +582,11 @@ def run_ours(a, cfg):
                     "hbm_frac": ab / (ctx_attn_ms * 1e-3) / 1e9 / hbm,
                     "roofline_us": max(ab / (hbm * 1e9), af / (tc * 1e12)) * 1e6,
                     "note": "tt_context_block_attn on the same inputs; timed separately, not in the step"},
+                "masked_nll": {
+                    "us": nll_ms * 1e3, "gbs": ub / (nll_ms * 1e-3) / 1e9, "hbm_frac": ub / (nll_ms * 1e-3) / 1e9 / hbm,
+                    "roofline_us": ub / (hbm * 1e9) * 1e6,
+                    "note": "tt_masked_nll over the step's logits with every position masked; timed separately, "
+                            "not in the step"},
                 "step_roofline_us": step_roof_us, "step_frac": step_roof_us / (ms / a.steps * 1e3)},
             "gpu_launches": a.steps * launches_per_step(cfg),
             "graph": use_graph,

@@ -24,7 +24,8 @@ STATUS_NAMES = {
 
 # Every symbol the header declares, in declaration order.
 EXPORTED = ("tt_status_string", "tt_version", "tt_denoise_attn_workspace_size", "tt_denoise_attn",
-            "tt_context_block_attn", "tt_unmask_workspace_size", "tt_unmask", "tt_unmask_noalloc", "tt_kv_append",
+            "tt_context_block_attn", "tt_unmask_workspace_size", "tt_unmask", "tt_unmask_noalloc",
+            "tt_linear_schedule_mask", "tt_masked_nll_workspace_size", "tt_masked_nll", "tt_kv_append",
             "tt_block_step_workspace_size", "tt_block_step", "tt_get_device_error", "tt_check_wait_timeout")
 
 
@@ -74,6 +75,9 @@ _SIGNATURES = {
     "tt_unmask_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
     "tt_unmask": (_I, [_P, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tt_unmask_noalloc": (_I, [_P, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "tt_linear_schedule_mask": (_I, [_P, _P, _P, _I, _I, ctypes.c_int32, _P, _P, _P, _P]),
+    "tt_masked_nll_workspace_size": (_I, [_I, _I, _I, _I, _PSZ]),
+    "tt_masked_nll": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tt_kv_append": (_I, [ctypes.POINTER(tt_kv_cache), _I, _PP, _PP, _P, _I, _I, _P, _P]),
     "tt_block_step_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, _I, _PSZ]),
     "tt_block_step": (_I, [ctypes.POINTER(tt_kv_cache), _I, _PP, _PP, _PP, _PP, _P, _I, _I, _I, _I, _F, _I,

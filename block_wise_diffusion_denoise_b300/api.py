@@ -249,6 +249,67 @@ def tt_unmask_noalloc(logits: torch.Tensor, masked: torch.Tensor, tokens: torch.
             "tt_unmask_noalloc")
 
 
+def tt_linear_schedule_mask(u: torch.Tensor, t: torch.Tensor, masked: Optional[torch.Tensor] = None,
+                            clean: Optional[torch.Tensor] = None, mask_id: int = -1,
+                            noisy: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Linear-schedule corruption: masked[b,p] = u[b,p] < t[b]; with ``noisy`` (and ``clean``)
+    also noisy = mask_id where masked, clean elsewhere.  u [B,S] fp32, t [B] fp32."""
+    B, S = u.shape
+    _need(u, "u", torch.float32, (B, S))
+    _need(t, "t", torch.float32, (B,))
+    if masked is None:
+        masked = torch.empty((B, S), dtype=torch.uint8, device=u.device)
+    _need(masked, "masked", torch.uint8, (B, S))
+    _need(clean, "clean", torch.int32, (B, S), allow_none=True)
+    _need(noisy, "noisy", torch.int32, (B, S), allow_none=True)
+    err = _err(dev_err)
+    N.check(N.lib().tt_linear_schedule_mask(_ptr(clean), u.data_ptr(), t.data_ptr(), B, S, int(mask_id),
+                                            _ptr(noisy), masked.data_ptr(), err, _stream(stream)),
+            "tt_linear_schedule_mask")
+    return masked
+
+
+def tt_masked_nll_workspace_size(B: int, S: int, V: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_size_t(0)
+    N.check(N.lib().tt_masked_nll_workspace_size(B, S, V, _DT[dtype], ctypes.byref(n)),
+            "tt_masked_nll_workspace_size")
+    return int(n.value)
+
+
+def tt_masked_nll(logits: torch.Tensor, targets: torch.Tensor, masked: torch.Tensor,
+                  nll: Optional[torch.Tensor] = None, nll_sum: Optional[torch.Tensor] = None,
+                  count: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                  dev_err: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Masked-diffusion loss: logits [B,S,V]; targets [B,S] int32; masked [B,S] uint8.
+    Returns (nll [B,S] fp32, NaN where unmasked; nll_sum [B] fp32; count [B] int32)."""
+    B, S, V = logits.shape
+    if logits.dtype not in _DT:
+        raise ValueError("logits must be bf16 or fp32")
+    _need(logits, "logits")
+    _need(targets, "targets", torch.int32, (B, S))
+    _need(masked, "masked", torch.uint8, (B, S))
+    dev = logits.device
+    if nll is None:
+        nll = torch.empty((B, S), dtype=torch.float32, device=dev)
+    if nll_sum is None:
+        nll_sum = torch.empty((B,), dtype=torch.float32, device=dev)
+    if count is None:
+        count = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(nll, "nll", torch.float32, (B, S))
+    _need(nll_sum, "nll_sum", torch.float32, (B,))
+    _need(count, "count", torch.int32, (B,))
+    err = _err(dev_err)
+    if ws is None:
+        ws = workspace(tt_masked_nll_workspace_size(B, S, V, logits.dtype), dev)
+    wp, wb = _ws(ws)
+    N.check(N.lib().tt_masked_nll(logits.data_ptr(), _DT[logits.dtype], B, S, V, targets.data_ptr(),
+                                  masked.data_ptr(), nll.data_ptr(), nll_sum.data_ptr(), count.data_ptr(),
+                                  wp, wb, err, _stream(stream)),
+            "tt_masked_nll")
+    return nll, nll_sum, count
+
+
 def tt_kv_append(caches: Sequence[KVCache], k_new: Sequence[torch.Tensor], v_new: Sequence[torch.Tensor],
                  seq_active: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> None:

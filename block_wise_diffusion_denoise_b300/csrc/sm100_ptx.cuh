@@ -57,6 +57,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
+// Warp-uniform form of mbar_wait: every lane polls (so every lane observes the phase and
+// its data), and the loop ends for all lanes together -- true once every lane has seen the
+// phase complete, false for all after `limit` rounds.  Call with the whole warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    bool done = false;
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (!done) done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Warp-uniform wait that naps between polls: every lane polls (so every lane observes the
+// phase and its data), a poll that fails is followed by a sleep of nap_ns (a waiting warp
+// then takes few issue slots, and wakes within about that time), the loop ends for all
+// lanes together, and it gives up (false in every lane) once limit_ns of wall time have
+// passed -- a bound on time, not on polls.  Call with the whole warp.
+__device__ __forceinline__ bool mbar_wait_warp_nap(uint64_t *bar, uint32_t parity, uint32_t nap_ns,
+                                                   uint64_t limit_ns) {
+    bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    uint64_t t0 = 0;
+    if ((threadIdx.x & 31) == 0) t0 = global_ns();
+    t0 = __shfl_sync(0xffffffffu, t0, 0);
+    for (;;) {
+        __nanosleep(nap_ns);
+        if (!done) done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        uint64_t t = 0;
+        if ((threadIdx.x & 31) == 0) t = global_ns();
+        if (__shfl_sync(0xffffffffu, t, 0) - t0 > limit_ns) return false;
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
@@ -218,6 +258,14 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Load with acquire semantics at GPU scope: orders the caller's later reads after the
+// writes released by whoever wrote (or extended the release sequence of) the value read.
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *ptr) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
 }
 
 // Fetch-and-add with acquire-release semantics at GPU scope: releases the calling

@@ -143,7 +143,7 @@ tt_status tt_unmask(const void *logits, tt_dtype dtype, int B, int S, int V, flo
     const size_t need = unmask_ws_bytes(B, S, V, dtype);
     if (ws == nullptr || ws_bytes < need) return TT_ERR_CAPACITY;
     if (reinterpret_cast<uintptr_t>(ws) % 16 != 0) return TT_ERR_UNSUPPORTED;
-    if (B > 65535) return TT_ERR_UNSUPPORTED;
+    if (B > 65535) return TT_ERR_UNSUPPORTED;   // the chunked kernel's grid limit
     return launch_unmask(logits, dtype, B, S, V, tau, step, T, masked, tokens, committed_now, conf,
                          n_masked, ws, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -159,6 +159,40 @@ tt_status tt_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S, in
     if (B > 65535) return TT_ERR_UNSUPPORTED;
     return launch_unmask_noalloc(logits, dtype, B, S, V, tau, step, T, masked, tokens, committed_now, conf,
                                  n_masked, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tt_status tt_linear_schedule_mask(const int32_t *clean, const float *u, const float *t, int B, int S,
+                                  int32_t mask_id, int32_t *noisy, uint8_t *masked, uint32_t *dev_err,
+                                  tt_stream_t stream) {
+    if (B < 0 || S < 1) return TT_ERR_INVALID_ARG;
+    if (B == 0) return TT_OK;
+    if (u == nullptr || t == nullptr || masked == nullptr || (noisy != nullptr && clean == nullptr))
+        return TT_ERR_INVALID_ARG;
+    return launch_linear_schedule(clean, u, t, B, S, mask_id, noisy, masked, dev_err,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+tt_status tt_masked_nll_workspace_size(int B, int S, int V, tt_dtype dtype, size_t *bytes) {
+    if (bytes == nullptr) return TT_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (B < 0 || S < 1 || V < 1 || !dtype_ok(dtype)) return TT_ERR_INVALID_ARG;
+    if (S > kMaxS) return TT_ERR_UNSUPPORTED;
+    *bytes = masked_nll_ws_bytes(B, S, V, dtype);
+    return TT_OK;
+}
+
+tt_status tt_masked_nll(const void *logits, tt_dtype dtype, int B, int S, int V, const int32_t *targets,
+                        const uint8_t *masked, float *nll, float *nll_sum, int32_t *count, void *ws,
+                        size_t ws_bytes, uint32_t *dev_err, tt_stream_t stream) {
+    if (B < 0 || S < 1 || V < 1 || !dtype_ok(dtype)) return TT_ERR_INVALID_ARG;
+    if (S > kMaxS) return TT_ERR_UNSUPPORTED;
+    if (B == 0) return TT_OK;
+    if (logits == nullptr || targets == nullptr || masked == nullptr) return TT_ERR_INVALID_ARG;
+    const size_t need = masked_nll_ws_bytes(B, S, V, dtype);
+    if (ws == nullptr || ws_bytes < need) return TT_ERR_CAPACITY;
+    if (reinterpret_cast<uintptr_t>(ws) % 16 != 0) return TT_ERR_UNSUPPORTED;
+    return launch_masked_nll(logits, dtype, B, S, V, targets, masked, nll, nll_sum, count, ws, dev_err,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 tt_status tt_kv_append(const tt_kv_cache *layers, int n_layers, const void *const *k_new,

@@ -31,6 +31,15 @@ tt_status launch_unmask_noalloc(const void *logits, tt_dtype dtype, int B, int S
                                 uint8_t *committed_now, float *conf, int32_t *n_masked,
                                 uint32_t *dev_err, cudaStream_t stream);
 
+// ---------------------------------------------------------------- masked-diffusion loss
+size_t masked_nll_ws_bytes(int B, int S, int V, tt_dtype dtype);
+tt_status launch_masked_nll(const void *logits, tt_dtype dtype, int B, int S, int V, const int32_t *targets,
+                            const uint8_t *masked, float *nll, float *nll_sum, int32_t *count, void *ws,
+                            uint32_t *dev_err, cudaStream_t stream);
+tt_status launch_linear_schedule(const int32_t *clean, const float *u, const float *t, int B, int S,
+                                 int32_t mask_id, int32_t *noisy, uint8_t *masked, uint32_t *dev_err,
+                                 cudaStream_t stream);
+
 // ---------------------------------------------------------------- append
 tt_status launch_kv_append(const tt_kv_cache *layers, int n_layers, const void *const *k_new,
                            const void *const *v_new, const uint8_t *seq_active, int B, int S,

@@ -1,7 +1,8 @@
 """Seeded synthetic inputs for one TwoTower denoiser step.
 
 This module only *draws* inputs: query/key/value tensors, paged context KV
-caches with shuffled page order, block KV and vocabulary logits.  It contains
+caches with shuffled page order, block KV, vocabulary logits, and the clean
+tokens, uniform draws and diffusion times of the training-side corruption.  It contains
 none of the step's arithmetic (no attention, no softmax, no unmasking rule), so
 that the float64 oracle and the CUDA path can both consume the very same values
 without sharing any of the code under test.
@@ -33,7 +34,8 @@ from typing import Optional
 import numpy as np
 
 # tensor ids used in the seed sequence
-T_Q, T_KBLK, T_VBLK, T_KPOOL, T_VPOOL, T_LOGITS, T_PAGES, T_LENS, T_KNEW, T_VNEW, T_PLANT = range(11)
+T_Q, T_KBLK, T_VBLK, T_KPOOL, T_VPOOL, T_LOGITS, T_PAGES, T_LENS, T_KNEW, T_VNEW, T_PLANT, \
+    T_UNIFORM, T_TIME, T_CLEAN = range(14)
 
 
 def rng_for(seed: int, config_id: int, block: int = 0, step: int = 0, layer: int = 0,
@@ -256,3 +258,13 @@ def _decode(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return (x.astype(np.uint32) << 16).view(np.float32)
     return np.asarray(x, dtype=np.float32)
+
+
+def draw_corruption(cfg: StepConfig, seed: int = 0, block: int = 0):
+    """Inputs of the masked-diffusion corruption of one batch of clean blocks: clean tokens
+    [B,S] ~ uniform over the vocabulary, uniform draws u [B,S] ~ U[0, 1) and one diffusion
+    time t [B] ~ U[0, 1] per sequence (float32)."""
+    clean = rng_for(seed, cfg.config_id, block, 0, 0, T_CLEAN).integers(0, cfg.V, size=(cfg.B, cfg.S))
+    u = rng_for(seed, cfg.config_id, block, 0, 0, T_UNIFORM).random((cfg.B, cfg.S), dtype=np.float32)
+    t = rng_for(seed, cfg.config_id, block, 0, 0, T_TIME).random(cfg.B, dtype=np.float32)
+    return clean.astype(np.int32), u, t

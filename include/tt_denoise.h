@@ -8,6 +8,9 @@
  *   tt_unmask        confidence unmasking of the block over the vocabulary logits
  *   tt_kv_append     commit of a finished block's KV into the context caches
  *   tt_block_step    all attention layers of one step followed by the unmasking
+ * and, on the training side of the same method:
+ *   tt_linear_schedule_mask  corruption of clean blocks under the linear schedule
+ *   tt_masked_nll    the masked-diffusion loss over the vocabulary logits
  *
  * Sources.  The method is described by the pages on "Nemotron-TwoTower:
  * Diffusion Language Modeling with Pretrained Autoregressive Context":
@@ -24,6 +27,10 @@
  *           and "Der Konfidenz-Trick": all masked tokens are predicted in
  *           parallel, those whose confidence exceeds a threshold are committed
  *           and locked, the rest stay masked for the next step.
+ *   [T]     same page, "Training und Konditionierung -- Maskierte Diffusion": clean
+ *           blocks are corrupted by replacing tokens with [MASK] under a linear
+ *           schedule, and the denoiser minimises the negative log-likelihood of the
+ *           original tokens at the masked positions.
  *   [NEWS]  dgnews.ru article, "How the architecture actually works": inside the
  *           block every masked position attends to every other block position,
  *           towards earlier blocks and the prompt attention stays causal, and each
@@ -198,7 +205,7 @@ TT_API tt_status tt_unmask_workspace_size(int B, int S, int V, tt_dtype dtype, s
  * token and mask and gets committed_now = 0.  n_masked[b] = masked positions
  * left.  conf[b,p] is NaN for positions that were already locked.
  *
- * logits   device [B, S, V], dtype bf16 or fp32 (any finite values)
+ * logits   device [B, S, V], dtype bf16 or fp32 (finite, |value| < 2^127)
  * step     1-based step index; T >= 1 the step budget of a block
  * masked, tokens         device, in/out
  * committed_now          device [B,S] uint8 out (may be NULL)
@@ -243,6 +250,54 @@ TT_API tt_status tt_unmask_noalloc(const void *logits, tt_dtype dtype, int B, in
                                    int step, int T, uint8_t *masked, int32_t *tokens,
                                    uint8_t *committed_now, float *conf, int32_t *n_masked,
                                    uint32_t *dev_err, tt_stream_t stream);
+
+/* Corruption of clean blocks for the masked-diffusion objective ([T]: clean blocks
+ * are corrupted by replacing tokens with [MASK] under a linear schedule).
+ *
+ * For every sequence b and position p: masked[b,p] = (u[b,p] < t[b]) -- each
+ * position is masked independently with probability t[b] when u is uniform on
+ * [0, 1) -- and, if noisy is not NULL, noisy[b,p] = mask_id where masked and
+ * clean[b,p] elsewhere.  The uniform draws are the caller's (no random numbers are
+ * drawn here).
+ *
+ * clean    device [B, S] int32 clean tokens (may be NULL when noisy is NULL)
+ * u        device [B, S] fp32 uniform draws
+ * t        device [B] fp32 diffusion times in [0, 1]; a sequence whose t lies
+ *          outside (or is NaN) sets TT_ERR_BOUNDS in dev_err and its outputs are
+ *          left untouched
+ * noisy    device [B, S] int32 out or NULL;  masked  device [B, S] uint8 out */
+TT_API tt_status tt_linear_schedule_mask(const int32_t *clean, const float *u, const float *t, int B, int S,
+                                         int32_t mask_id, int32_t *noisy, uint8_t *masked, uint32_t *dev_err,
+                                         tt_stream_t stream);
+
+/* Bytes of workspace tt_masked_nll needs (pure host arithmetic). */
+TT_API tt_status tt_masked_nll_workspace_size(int B, int S, int V, tt_dtype dtype, size_t *bytes);
+
+/* Masked-diffusion loss of the denoiser's logits ([T]: the negative
+ * log-likelihood of the original tokens at the masked positions).
+ *
+ * For every sequence b and position p with masked[b,p] != 0 and clean token
+ * x = targets[b,p]:
+ *   nll[b,p] = log sum_v exp(logits[b,p,v]) - logits[b,p,x]
+ *            = (m - logits[b,p,x]) + log sum_v exp(logits[b,p,v] - m),  m = max_v;
+ * nll_sum[b] = the sum of nll over the masked positions of b (no weighting; a
+ * caller may weight per sequence), count[b] = their number.  Positions that are
+ * not masked get nll = NaN and their logits are never read.
+ *
+ * logits   device [B, S, V], bf16 or fp32, finite with |value| < 2^127; the rows
+ *          must be 16-byte aligned (base address and V * element size a multiple
+ *          of 16), else TT_ERR_UNSUPPORTED
+ * targets  device [B, S] int32; a masked position whose target lies outside
+ *          [0, V) gets NaN and sets TT_ERR_BOUNDS in dev_err
+ * masked   device [B, S] uint8 (as written by tt_linear_schedule_mask)
+ * nll      device [B, S] fp32 out or NULL;  nll_sum  device [B] fp32 out or NULL;
+ * count    device [B] int32 out or NULL
+ * ws, ws_bytes  device workspace of at least tt_masked_nll_workspace_size bytes,
+ *          zero-filled before its first use (left zeroed by every call)
+ * Arithmetic: fp32; |nll - exact| <= 1e-5 * max(1, |nll|). */
+TT_API tt_status tt_masked_nll(const void *logits, tt_dtype dtype, int B, int S, int V, const int32_t *targets,
+                               const uint8_t *masked, float *nll, float *nll_sum, int32_t *count, void *ws,
+                               size_t ws_bytes, uint32_t *dev_err, tt_stream_t stream);
 
 /* Commit of a finished block into the context caches of n_layers layers ([GEN]:
  * the context tower extends its state with the clean tokens).

@@ -111,6 +111,38 @@ def test_unmask_rejects_bad_arguments_on_the_host(lib):
     assert call(B=0) == N.TT_OK
 
 
+def test_masked_nll_and_schedule_reject_bad_arguments_on_the_host(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.tt_masked_nll_workspace_size(32, 16, 131072, N.TT_BF16, ctypes.byref(n)) == N.TT_OK
+    # 4 units of 64 KB per row in blocks of 2: 2 partials of 16 bytes per row, plus tickets
+    assert n.value >= 32 * 16 * 2 * 16 + 32 * 4
+    assert lib.tt_masked_nll_workspace_size(1, 0, 10, N.TT_BF16, ctypes.byref(n)) == N.TT_ERR_INVALID_ARG
+    assert lib.tt_masked_nll_workspace_size(1, 16, 10, 5, ctypes.byref(n)) == N.TT_ERR_INVALID_ARG
+
+    def call(logits=0x10000, dtype=N.TT_BF16, B=2, S=16, V=1024, targets=0x20000, masked=0x30000, ws=0x40000,
+             ws_bytes=1 << 20):
+        return lib.tt_masked_nll(logits, dtype, B, S, V, targets, masked, None, None, None, ws, ws_bytes, None,
+                                 None)
+    assert call(targets=0) == N.TT_ERR_INVALID_ARG
+    assert call(masked=0) == N.TT_ERR_INVALID_ARG
+    assert call(logits=0) == N.TT_ERR_INVALID_ARG
+    assert call(V=0) == N.TT_ERR_INVALID_ARG
+    assert call(ws=0) == N.TT_ERR_CAPACITY
+    assert call(ws_bytes=64) == N.TT_ERR_CAPACITY
+    assert call(S=2048) == N.TT_ERR_UNSUPPORTED
+    assert call(V=1003) == N.TT_ERR_UNSUPPORTED            # rows not 16-byte aligned
+    assert call(logits=0x10002) == N.TT_ERR_UNSUPPORTED
+    assert call(B=0) == N.TT_OK
+    # the corruption step
+    sched = lib.tt_linear_schedule_mask
+    assert sched(None, 0, 0x2000, 2, 16, -1, None, 0x3000, None, None) == N.TT_ERR_INVALID_ARG      # no u
+    assert sched(None, 0x1000, 0, 2, 16, -1, None, 0x3000, None, None) == N.TT_ERR_INVALID_ARG      # no t
+    assert sched(None, 0x1000, 0x2000, 2, 16, -1, None, 0, None, None) == N.TT_ERR_INVALID_ARG      # no mask out
+    assert sched(None, 0x1000, 0x2000, 2, 16, -1, 0x4000, 0x3000, None, None) == N.TT_ERR_INVALID_ARG  # noisy, no clean
+    assert sched(None, 0x1000, 0x2000, 2, 0, -1, None, 0x3000, None, None) == N.TT_ERR_INVALID_ARG
+    assert sched(None, 0, 0, 0, 16, -1, None, 0, None, None) == N.TT_OK                             # empty batch
+
+
 def test_append_rejects_bad_arguments_on_the_host(lib):
     two = (N.tt_kv_cache * 2)(_cache(), _cache(ctx_len=0x5000))
     kn = N.ptr_array([0x10000, 0x11000])

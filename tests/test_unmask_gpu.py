@@ -117,9 +117,11 @@ def test_locked_rows_are_never_read_and_ties_take_lowest_id(stats):
         stats += support.compare_unmask(masked, tokens, ora, *g, cfg.tau, step, cfg.T)
 
 
-@pytest.mark.parametrize("V", [1, 7, 1003, 16384, 16385, 50001])
+@pytest.mark.parametrize("V", [1, 7, 8, 1003, 4100, 8200, 16384, 16385, 16392, 40000, 50001])
 def test_ragged_vocab_sizes(V, stats):
-    """Vocabulary sizes that are not a multiple of the vector width or of the chunk."""
+    """Vocabulary sizes that are not a multiple of the vector width (unaligned rows: the chunked
+    kernel) or of the streaming pass's 16 KB unit and 4-unit block (aligned rows: a partial last
+    unit, a partial last block)."""
     for dtype in ("bf16", "f32"):
         cfg = synth.CONFIGS["tiny"].replace(B=2, V=V, dtype=dtype)
         lg = synth.draw_logits(cfg, seed=V, peak_hi=20.0)
@@ -142,9 +144,9 @@ def test_nothing_masked_and_empty_batch():
     torch.cuda.synchronize()
 
 
-def test_large_batch_runs_the_chunked_kernel(stats):
-    """B*S above the streaming kernel's row list (4096 rows) takes the chunked kernel; mixed
-    masked rows, every branch of the rules, bit-exact against the oracle."""
+def test_large_batch(stats):
+    """260 sequences (4160 rows, more blocks than the grid has CTAs many times over); mixed
+    masked rows, a few sequences with nothing masked, every branch of the rules."""
     cfg = synth.CONFIGS["single"].replace(B=260, V=4096)
     rng = np.random.default_rng(4)
     lg = synth.draw_logits(cfg, seed=13, peak_hi=30.0)

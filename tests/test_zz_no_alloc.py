@@ -48,8 +48,8 @@ def _outputs(cfg, dtype, lg_dev, masked, tokens, step, noalloc):
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,dtype", [("ctx8k", "bf16"), ("tiny", "f32"), ("large_batch", "f32")])
 def test_noalloc_matches_workspace_entry_point_twice(name, dtype):
-    """ctx8k takes the streaming kernel at full vocabulary; large_batch (260 sequences x 16
-    positions, above the streaming kernel's 4096-row list, V = 1024) takes the chunked one."""
+    """ctx8k: full vocabulary; tiny: fp32; large_batch: 260 sequences x 16 positions at V = 1024,
+    many more blocks than CTAs."""
     if name == "large_batch":
         cfg = synth.CONFIGS["single"].replace(B=260, V=1024, dtype=dtype)
     else:
