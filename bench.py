@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 from block_wise_diffusion_denoise_b300 import synth  # noqa: E402
 
 WORKLOADS = {
-    "ctx8k": "ctx8k", "single": "single", "ragged": "ragged", "long": "long",
+    "ctx8k": "ctx8k", "single": "single", "ragged": "ragged", "long": "long", "loop": "loop",
 }
 
 
@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--s-variants", action="store_true",
+                    help="also time the attention at block sizes S = 32, 64, 128 on the same contexts")
     return ap.parse_args()
 
 
@@ -92,6 +94,17 @@ def attn_bytes(cfg, lens) -> float:
 
 def attn_flops(cfg, lens) -> float:
     return float(sum(4.0 * cfg.Hq * cfg.S * cfg.D * (int(L) + cfg.S) for L in lens))
+
+
+def s_var_entry(cfg, lens, Sv, us, hbm, tc):
+    """Timing of the attention at block size Sv against its own roofline (bytes grow a little with
+    S, flops in proportion: from S = 32 on the tensor bound takes over)."""
+    c2 = cfg.replace(S=Sv)
+    ab, af = attn_bytes(c2, lens), attn_flops(c2, lens)
+    t_hbm, t_tc = ab / (hbm * 1e9), af / (tc * 1e12)
+    roof = max(t_hbm, t_tc) * 1e6
+    return {"us": us, "roofline_us": roof, "bound": "hbm" if t_hbm >= t_tc else "tensor", "frac": roof / us,
+            "gbs": ab / (us * 1e-6) / 1e9, "tflops": af / (us * 1e-6) / 1e12}
 
 
 def unmask_bytes(cfg, masked_rows) -> float:
@@ -483,6 +496,23 @@ def run_ours(a, cfg):
     ctx_attn_ms = timed(ctx_attn_only, 0, k_ker, use_graph) / k_ker
     # the training-side loss over the same logits (not part of the denoise step)
     nll_ms = timed(nll_only, 0, k_ker, use_graph) / k_ker
+    # block sizes S = 32, 64, 128 on the same contexts (the attention alone)
+    s_var = {}
+    if a.s_variants:
+        for Sv in (32, 64, 128):
+            g = torch.Generator(device=dev)
+            g.manual_seed(Sv)
+            qv = (torch.randn((cfg.B, Sv, cfg.Hq, cfg.D), generator=g, device=dev) * scale).to(tdt)
+            kv_ = (torch.randn((cfg.B, Sv, cfg.Hkv, cfg.D), generator=g, device=dev) * scale).to(tdt)
+            vv_ = (torch.randn((cfg.B, Sv, cfg.Hkv, cfg.D), generator=g, device=dev) * scale).to(tdt)
+            ov = torch.empty_like(qv)
+            wsv = api.workspace(api.tt_denoise_attn_workspace_size(cfg.B, Sv, cfg.Hq, cfg.Hkv, cfg.D, tdt), dev)
+
+            def attn_sv(i, stream=None, qv=qv, kv_=kv_, vv_=vv_, ov=ov, wsv=wsv):
+                c = copies[i % n_copies]
+                api.tt_denoise_attn(c["cache"], qv, kv_, vv_, out=ov, sm_scale=scale, ws=wsv, dev_err=err,
+                                    stream=stream)
+            s_var[Sv] = timed(attn_sv, 0, k_ker, use_graph) / k_ker
     if api.tt_get_device_error(err) != 0:
         raise SystemExit("device error in the per-kernel timings")
 
@@ -588,6 +618,8 @@ def run_ours(a, cfg):
                     "note": "tt_masked_nll over the step's logits with every position masked; timed separately, "
                             "not in the step"},
                 "step_roofline_us": step_roof_us, "step_frac": step_roof_us / (ms / a.steps * 1e3)},
+            "attention_block_sizes": {
+                f"S{Sv}": s_var_entry(cfg, lens, Sv, us * 1e3, hbm, tc) for Sv, us in s_var.items()},
             "gpu_launches": a.steps * launches_per_step(cfg),
             "graph": use_graph,
             "clocks": sampler.summary(),
@@ -606,6 +638,199 @@ def run_ours(a, cfg):
     return 0
 
 
+# --------------------------------------------------------------------------- the block loop
+
+def run_loop(a, cfg):
+    """The full block loop: B sequences with their own paged caches in every one of n_layers
+    attention layers, n_blocks consecutive blocks of S positions, each refined for T steps
+    (tt_block_step: every layer's attention, then the unmasking of the step's logits) and then
+    committed into every layer's cache (tt_kv_append), all replayed from one CUDA graph.
+
+    Values: pools and block q/k/v ~ N(0,1)/sqrt(D), step logits ~ N(0,3) plus a peak U[0,12]
+    at a uniform token per position, committed-block K/V ~ N(0,1), all drawn on the device
+    from torch generators seeded by (seed, block, step, layer); page tables from synth."""
+    import torch
+    import torch.distributed as dist
+
+    from block_wise_diffusion_denoise_b300 import api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    bf = torch.bfloat16
+    seed = a.seed + 1000 * rank
+    B, S, Hq, Hkv, D, V, T, NL, NB = cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.D, cfg.V, cfg.T, cfg.n_layers, cfg.n_blocks
+    L0 = cfg.len_lo
+    cap = L0 + S * NB
+    table_h, num_pages = synth.draw_page_table(cfg, cap, seed)
+    table = torch.from_numpy(table_h).to(dev)
+    ctx0 = torch.full((B,), L0, dtype=torch.int32, device=dev)
+    ctx_len = ctx0.clone()
+
+    import zlib
+
+    def gen(*key):
+        g = torch.Generator(device=dev)
+        g.manual_seed(zlib.crc32(repr((seed,) + key).encode()))
+        return g
+
+    def normal(shape, scale, key):
+        return (torch.randn(shape, generator=gen(*key), device=dev, dtype=torch.float32) * scale).to(bf)
+
+    sc = 1.0 / math.sqrt(D)
+    caches = [api.KVCache(normal((num_pages, Hkv, cfg.page_size, D), sc, ("k", l)),
+                          normal((num_pages, Hkv, cfg.page_size, D), sc, ("v", l)), table, ctx_len)
+              for l in range(NL)]
+    # block q/k/v: two rotating sets per layer (their values do not change the work)
+    qkv = [[(normal((B, S, Hq, D), sc, ("q", l, r)), normal((B, S, Hkv, D), sc, ("kb", l, r)),
+             normal((B, S, Hkv, D), sc, ("vb", l, r))) for l in range(NL)] for r in range(2)]
+    outs = [torch.empty((B, S, Hq, D), dtype=bf, device=dev) for _ in range(NL)]
+    logits = []
+    for blk in range(NB):
+        for st in range(T):
+            g = gen("lg", blk, st)
+            x = torch.randn((B, S, V), generator=g, device=dev, dtype=torch.float32) * cfg.logit_std
+            tok = torch.randint(0, V, (B, S), generator=g, device=dev)
+            h = torch.rand((B, S), generator=g, device=dev) * cfg.peak_hi
+            x.view(B * S, V)[torch.arange(B * S, device=dev), tok.view(-1)] += h.view(-1)
+            logits.append(x.to(bf))
+            del x
+    knew = [[normal((B, S, Hkv, D), 1.0, ("kn", blk, l)) for l in range(NL)] for blk in range(NB)]
+    vnew = [[normal((B, S, Hkv, D), 1.0, ("vn", blk, l)) for l in range(NL)] for blk in range(NB)]
+    masked = torch.ones((B, S), dtype=torch.uint8, device=dev)
+    tokens = torch.full((B, S), -1, dtype=torch.int32, device=dev)
+    nsteps = NB * T
+    com = torch.zeros((nsteps, B, S), dtype=torch.uint8, device=dev)
+    nm = torch.zeros((nsteps, B), dtype=torch.int32, device=dev)
+    ws = api.workspace(api.tt_block_step_workspace_size(B, S, Hq, Hkv, D, V, bf), dev)
+    err = api.error_word(dev)
+
+    def loop(stream):
+        ctx_len.copy_(ctx0)
+        for blk in range(NB):
+            masked.fill_(1)
+            tokens.fill_(-1)
+            for st in range(1, T + 1):
+                i = blk * T + st - 1
+                r = qkv[i % 2]
+                api.tt_block_step(caches, [x[0] for x in r], [x[1] for x in r], [x[2] for x in r], outs, logits[i],
+                                  masked, tokens, cfg.tau, st, T, sm_scale=sc, committed_now=com[i],
+                                  n_masked=nm[i], ws=ws, dev_err=err, stream=stream)
+            api.tt_kv_append(caches, knew[blk], vnew[blk], dev_err=err, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    s_ = torch.cuda.Stream(device=dev)
+    s_.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s_):
+        loop(s_)                                        # eager warm-up (and first check)
+    barrier()
+    if api.tt_get_device_error(err) != 0:
+        raise SystemExit("device error in the block loop")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s_):
+        loop(s_)
+    for _ in range(max(1, a.warmup)):
+        g.replay()
+    barrier()
+    reps = max(1, a.steps // nsteps) if a.steps >= nsteps else 1
+    sampler = ClockSampler(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler, torch.cuda.stream(s_):
+        ev0.record(s_)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(s_)
+        ev1.synchronize()
+    barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    if api.tt_get_device_error(err) != 0:
+        raise SystemExit("device error in the timed block loop")
+    # every block finished within T steps and every step committed at least one position
+    ends = nm.view(NB, T, B)[:, T - 1]
+    if int(ends.max().item()) != 0:
+        raise SystemExit("a block did not finish within T steps")
+    commits = com.view(NB, T, B, S).sum(dim=(2, 3)).float()    # per (block, step), whole batch
+    steps_done = (commits > 0).sum().item()
+
+    # the append alone: NB appends from the start length, timed in a graph
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ga, stream=s_):
+        ctx_len.copy_(ctx0)
+        for blk in range(NB):
+            api.tt_kv_append(caches, knew[blk], vnew[blk], dev_err=err, stream=s_)
+    ga.replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s_):
+        e0.record(s_)
+        for _ in range(10):
+            ga.replay()
+        e1.record(s_)
+        e1.synchronize()
+    append_us = e0.elapsed_time(e1) / (10 * NB) * 1e3
+
+    if rank == 0:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+            if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+        hbm = peaks.get("hbm_gbs", 6400.0)
+        tc = peaks.get("bf16_tflops", 1800.0)
+        # algorithmic cost of the whole loop (every layer's attention at the block's context
+        # length; the unmasking reads every still-masked row; the append moves S rows per layer)
+        roof_s = 0.0
+        byts = 0.0
+        mask_rows = nm.view(NB, T, B).sum(dim=2).cpu().numpy()
+        for blk in range(NB):
+            lens = np.full(B, L0 + S * blk)
+            ab, af = attn_bytes(cfg, lens), attn_flops(cfg, lens)
+            for st in range(T):
+                masked_before = B * S if st == 0 else int(mask_rows[blk, st - 1])
+                ub = unmask_bytes(cfg, masked_before)
+                roof_s += NL * max(ab / (hbm * 1e9), af / (tc * 1e12)) + ub / (hbm * 1e9)
+                byts += NL * ab + ub
+            append_b = NL * 2 * 2 * B * S * Hkv * D * 2.0          # read + write, K and V
+            roof_s += append_b / (hbm * 1e9)
+            byts += append_b
+        per_loop_ms = ms / reps
+        value = job_rate(world, reps * nsteps, ms)
+        line = {
+            "metric": "block-loop denoise steps/s (6 attention layers + unmask per step, append per block)",
+            "value": value, "unit": "steps/s", "n_gpus": world, "steps": reps * nsteps, "warmup": a.warmup,
+            "ms_per_step": per_loop_ms / nsteps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded on the device; value distributions of the workload recipe)",
+            "config": {"workload": f"loop: B={B}, initial context {L0}, S={S}, {Hq}q/{Hkv}kv heads, head_dim {D}, "
+                                   f"vocab {V}, {NL} attention layers with their own paged caches, {NB} blocks of "
+                                   f"T={T} steps, tau={cfg.tau}, tt_kv_append per block",
+                       "l2": "inputs larger than L2 (1.6 GB of caches, 64 MB of logits per step)"},
+            "roofline": {"bound": "hbm", "achieved": byts / (per_loop_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": roof_s / (per_loop_ms * 1e-3), "peak_source": "of measured" if peaks else "of fallback",
+                         "roofline_ms_per_loop": roof_s * 1e3, "algorithmic_bytes_per_loop": byts},
+            "commits_per_step": float(commits.sum().item() / nsteps),
+            "commits_per_step_per_sequence": float(commits.sum().item() / nsteps / B),
+            "steps_with_a_commit": int(steps_done),
+            "kernels": {"append": {"us": append_us, "layers": NL,
+                                   "bytes": NL * 2 * 2 * B * S * Hkv * D * 2.0,
+                                   "gbs": NL * 2 * 2 * B * S * Hkv * D * 2.0 / (append_us * 1e-6) / 1e9}},
+            "gpu_launches": reps * (nsteps * (NL + 1) + NB),
+            "graph": True,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def launches_per_step(cfg) -> int:
     return 2          # one attention kernel + one unmask kernel
 
@@ -615,6 +840,8 @@ def main():
     cfg = synth.CONFIGS[WORKLOADS[a.config]]
     if a.impl == "reference":
         return run_reference(a, cfg)
+    if a.config == "loop":
+        return run_loop(a, cfg)
     return run_ours(a, cfg)
 
 
