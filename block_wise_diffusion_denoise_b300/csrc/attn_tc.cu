@@ -67,6 +67,7 @@
 #include "sm100_ptx.cuh"
 #include "tt_common.cuh"
 #include "tt_internal.h"
+#include "attn_work.cuh"
 
 namespace tt {
 namespace {
@@ -74,26 +75,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kD = 128;                  // head dim
-constexpr int kPage = 64;                // tokens per page
-constexpr int kTileKeys = 128;           // keys per context tile (two pages)
 constexpr int kKStages = 3;              // K ring depth (K is needed first: QK starts a tile)
 constexpr int kVStages = 3;              // V ring depth (a V stage is held until PV completes)
 constexpr int kMaxCtas = 296;            // upper bound of the persistent grid (sizes the workspace)
 constexpr uint32_t kWaitLimit = 1u << 20;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-// Work units of the stream-K split: a context tile costs kCostTile, the block tile
-// kCostBlock (its MMAs are short but its softmax is a full tile's), and every segment
-// carries kCostSeg up front for what a piece boundary costs (Q load, pipeline refill,
-// epilogue and, for split segments, the merge).
-constexpr int kCostTile = 8, kCostBlock = 6, kCostSeg = 24;
-// Splitting a segment between groups costs about this many units more than it saves
-// (a second piece boundary, the partial write and the merge): when every group can take
-// a whole segment and the longest one is within this margin of the even split, each
-// group takes one whole segment instead.
-constexpr int kCostSplit = 80;
-// A stream-K group gets at least this many units (eight tiles) of work.
-constexpr int kMinGroupUnits = 64;
-
 // Shared memory (offsets from a 1024-byte aligned base).  Every 128-row operand is
 // stored as two 128-byte-swizzled halves of 64 columns (d 0..63 and d 64..127).
 constexpr int kHalf = 16384;             // 128 rows x 128 bytes
@@ -159,112 +145,6 @@ struct Shared {
     int max_len;           // longest context of the launch
 };
 
-// ------------------------------------------------------------------ work partition
-
-__device__ __forceinline__ int seq_cost(int L, int Hkv) {
-    return Hkv * (kCostSeg + kCostTile * ((L + kTileKeys - 1) / kTileKeys) + kCostBlock);
-}
-
-struct Piece {
-    int b, g, sg;          // sequence, KV head, segment index b * Hkv + g
-    int L, ntc;            // context length and its tiles (tile ntc is the block tile)
-    int first, last;       // tiles [first, last) of this segment belong to this group
-    long long X;           // start unit of the segment
-    bool whole;
-};
-
-// Walks the pieces of one CTA group's cost range [lo, hi).  Tile i of a segment that
-// starts at unit X starts at unit X + kCostSeg + kCostTile * i (the block tile is i = ntc).
-struct WorkIter {
-    long long U, lo, hi, X;
-    int NG;                 // groups that share the work (the stream-K split's divisor)
-    int b, g, L, ntc, C;
-    int B, Hkv;
-    const long long *pre;   // shared: prefix sums of the sequences' work units
-    const int *lens;        // shared: clamped context lengths
-
-    __device__ void init(const TcParams &p, int group, const long long *pre_, const int *lens_, int max_len) {
-        B = p.B; Hkv = p.Hkv; pre = pre_; lens = lens_;
-        U = pre[B];
-        const long long nseg = (long long)B * Hkv;
-        const long long max_seg = seq_cost(max_len, 1);
-        NG = p.n_groups;
-        if (nseg <= p.n_groups && max_seg <= U / p.n_groups + kCostSplit) {
-            // one whole segment per group: the range of segment `group` exactly
-            if (group < nseg) {
-                const int sb = (int)(group / Hkv), sg = (int)(group % Hkv);
-                lo = pre[sb] + (long long)sg * seq_cost(lens[sb], 1);
-                hi = lo + seq_cost(lens[sb], 1);
-            } else {
-                lo = hi = U;
-            }
-        } else {
-            // stream-K over at most U / kMinGroupUnits groups, so that a small batch is not
-            // cut into one-tile pieces whose merges would cost more than the tiles
-            const long long ng = U / kMinGroupUnits;
-            NG = (int)(ng < 1 ? 1 : (ng < p.n_groups ? ng : p.n_groups));
-            if (group < NG) {
-                lo = (long long)group * U / NG;
-                hi = (long long)(group + 1) * U / NG;
-            } else {
-                lo = hi = U;
-            }
-        }
-        // the first sequence that ends after lo
-        int a = 0, z = B;
-        while (a < z) {
-            const int mid = (a + z) >> 1;
-            if (pre[mid + 1] > lo) z = mid; else a = mid + 1;
-        }
-        b = a; g = 0;
-        X = (b < B) ? pre[b] : U;
-        load(p);
-    }
-    __device__ void load(const TcParams &) {
-        if (b < B) {
-            L = lens[b];
-            ntc = (L + kTileKeys - 1) / kTileKeys;
-            C = kCostSeg + kCostTile * ntc + kCostBlock;
-        }
-    }
-    __device__ bool next(const TcParams &p, Piece &pc) {
-        while (b < B && X < hi) {
-            const long long T0 = X + kCostSeg;   // unit of tile 0
-            const long long first = (lo > T0) ? (lo - T0 + kCostTile - 1) / kCostTile : 0;
-            long long last = (hi > T0) ? (hi - T0 + kCostTile - 1) / kCostTile : 0;
-            if (last > ntc + 1) last = ntc + 1;
-            const bool have = first < last;
-            if (have) {
-                pc.b = b; pc.g = g; pc.sg = b * Hkv + g; pc.L = L; pc.ntc = ntc;
-                pc.first = (int)first; pc.last = (int)last; pc.X = X;
-                pc.whole = (first == 0 && last == ntc + 1);
-            }
-            X += C;
-            if (++g == Hkv) { g = 0; ++b; load(p); }
-            if (have) return true;
-        }
-        return false;
-    }
-};
-
-__device__ __forceinline__ long long range_lo(long long c, long long U, int n) { return c * U / n; }
-
-// The group whose range holds unit u.
-__device__ __forceinline__ int owner(long long u, long long U, int n) {
-    long long c = u * n / U;
-    while (c + 1 < n && range_lo(c + 1, U, n) <= u) ++c;
-    while (c > 0 && range_lo(c, U, n) > u) --c;
-    return (int)c;
-}
-
-// Does group c own at least one tile of the segment starting at unit X with ntc context tiles?
-__device__ __forceinline__ bool owns_tile(int c, long long X, int ntc, long long U, int n) {
-    const long long lo_c = range_lo(c, U, n), hi_c = range_lo(c + 1, U, n);
-    const long long T0 = X + kCostSeg;
-    const long long i0 = (lo_c > T0) ? (lo_c - T0 + kCostTile - 1) / kCostTile : 0;
-    return i0 <= ntc && T0 + kCostTile * i0 < hi_c;
-}
-
 // ------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, uint32_t *dev_err) {
@@ -295,29 +175,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // each (128 x 64 + 256 x 216 = 63488 <= 64512).
 __device__ __forceinline__ void regs_release() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;"); }
 __device__ __forceinline__ void regs_acquire() { asm volatile("setmaxnreg.inc.sync.aligned.u32 216;"); }
-
-// One elected lane of a converged warp issues each MMA, so the operands stay warp-uniform.
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred;
-    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
-    return pred != 0;
-}
-
-// Physical page of logical page pg of the piece's sequence (0 past the context; an id
-// outside the pool is reported and replaced by 0 so that no copy leaves the pool).
-__device__ __forceinline__ int page_id(const TcParams &p, const Piece &pc, int pg) {
-    if (pg * kPage >= pc.L) return 0;
-    const int id = p.page_table[(size_t)pc.b * p.max_pages + pg];
-    if (id < 0 || id >= p.num_pages) {
-        report_error(p.dev_err, TT_ERR_BOUNDS);
-        return 0;
-    }
-    return id;
-}
-
-__device__ __forceinline__ int tile_valid(const Piece &pc, int i, int S) {
-    return i < pc.ntc ? min(kTileKeys, pc.L - kTileKeys * i) : S;
-}
 
 // Scores at columns at or past `valid` become -inf (only the last context tile of a
 // segment and the block tile are partial), so one code path serves every tile.
@@ -899,33 +756,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-bool make_map(CUtensorMap *m, const void *ptr, int rank, const uint64_t *dims, const uint64_t *strides,
-              const uint32_t *box) {
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    cuuint64_t d[5], s[4];
-    cuuint32_t b[5], e[5];
-    for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; e[i] = 1; }
-    for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(ptr), d, s, b, e,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int rows_of(int S, int Hq, int Hkv) { return (Hq / Hkv) * S; }
 
 }  // namespace
@@ -960,13 +790,7 @@ tt_status launch_chunk(const AttnArgs &a, int b0, int nb, int sms) {
     const int rows = G * a.S;
     const int cps = rows / 128;   // CTAs per segment, one per 128-row M tile
     CUtensorMap mk, mv, mkb, mvb;
-    {
-        const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)kPage, (uint64_t)a.Hkv, (uint64_t)c.num_pages};
-        const uint64_t str[3] = {(uint64_t)kD * 2, (uint64_t)kPage * kD * 2, (uint64_t)a.Hkv * kPage * kD * 2};
-        const uint32_t box[4] = {64, (uint32_t)kPage, 1, 1};
-        if (!make_map(&mk, c.k_pool, 4, dims, str, box)) return TT_ERR_CUDA;
-        if (!make_map(&mv, c.v_pool, 4, dims, str, box)) return TT_ERR_CUDA;
-    }
+    if (!make_pool_maps(c, a.Hkv, &mk, &mv)) return TT_ERR_CUDA;
     {
         const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)nb * a.S};
         const uint64_t str[2] = {(uint64_t)kD * 2, (uint64_t)a.Hkv * kD * 2};

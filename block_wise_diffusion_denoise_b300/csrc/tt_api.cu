@@ -64,9 +64,10 @@ tt_status tt_denoise_attn_workspace_size(int B, int S, int Hq, int Hkv, int D, t
     *bytes = 0;
     const tt_status st = attn_shape(B, S, Hq, Hkv, D, dtype);
     if (st != TT_OK) return st;
-    // The tensor-core kernel needs split partials; page size is checked at call time,
-    // so size for it whenever the rest of the shape qualifies.
+    // The tensor-core kernels need split partials; page size is checked at call time,
+    // so size for them whenever the rest of the shape qualifies.
     if (attn_tc_supported(S, Hq, Hkv, D, 64, dtype)) *bytes = attn_tc_ws_bytes(B, S, Hq, Hkv, D);
+    if (attn_decode_supported(S, Hq, Hkv, D, 64, dtype)) *bytes = attn_decode_ws_bytes(B, Hkv);
     return TT_OK;
 }
 
@@ -98,6 +99,12 @@ tt_status attention(const tt_kv_cache *ctx, const void *q, const void *k_blk, co
         if (need > 0 && (ws == nullptr || ws_bytes < need)) return TT_ERR_CAPACITY;
         if (need > 0 && reinterpret_cast<uintptr_t>(ws) % 256 != 0) return TT_ERR_UNSUPPORTED;
         return launch_attn_tc(a);
+    }
+    if (attn_decode_supported(S, Hq, a.Hkv, a.D, ctx->page_size, (tt_dtype)ctx->dtype) && sm_scale > 0.f) {
+        const size_t need = attn_decode_ws_bytes(B, a.Hkv);
+        if (ws == nullptr || ws_bytes < need) return TT_ERR_CAPACITY;
+        if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return TT_ERR_UNSUPPORTED;
+        return launch_attn_decode(a);
     }
     return launch_attn_simt(a);
 }

@@ -67,6 +67,11 @@ bool attn_tc_supported(int S, int Hq, int Hkv, int D, int page_size, tt_dtype dt
 size_t attn_tc_ws_bytes(int B, int S, int Hq, int Hkv, int D);
 tt_status launch_attn_tc(const AttnArgs &a);
 
+// Single-position queries (S = 1) with 16 query heads per KV head: the decode kernel.
+bool attn_decode_supported(int S, int Hq, int Hkv, int D, int page_size, tt_dtype dtype);
+size_t attn_decode_ws_bytes(int B, int Hkv);
+tt_status launch_attn_decode(const AttnArgs &a);
+
 // One warp waits (bounded) on an mbarrier nothing arrives at and reports the timeout.
 tt_status launch_wait_check(uint32_t polls, uint32_t *dev_err, cudaStream_t stream);
 

@@ -52,6 +52,15 @@ def test_workspace_sizes(lib):
     assert lib.tt_denoise_attn_workspace_size(4, 16, 32, 2, 96, N.TT_BF16, ctypes.byref(n)) == N.TT_ERR_UNSUPPORTED
     assert lib.tt_denoise_attn_workspace_size(4, 16, 32, 2, 128, 7, ctypes.byref(n)) == N.TT_ERR_INVALID_ARG
     assert lib.tt_denoise_attn_workspace_size(4, 16, 32, 2, 128, N.TT_BF16, None) == N.TT_ERR_INVALID_ARG
+    # one position, 16 query heads per KV head: the decode kernel's split partials
+    # (O^T of 16 heads x 128 d, then 16 maxima and 16 sums) for every CTA and segment
+    assert lib.tt_denoise_attn_workspace_size(4, 1, 32, 2, 128, N.TT_BF16, ctypes.byref(n)) == N.TT_OK
+    assert n.value >= (296 + 8) * (16 * 128 + 32) * 4
+    # one position with another head ratio, or fp32: no tensor-core kernel, no workspace
+    assert lib.tt_denoise_attn_workspace_size(4, 1, 16, 2, 128, N.TT_BF16, ctypes.byref(n)) == N.TT_OK
+    assert n.value == 0
+    assert lib.tt_denoise_attn_workspace_size(4, 1, 32, 2, 128, N.TT_FP32, ctypes.byref(n)) == N.TT_OK
+    assert n.value == 0
     t = ctypes.c_size_t(0)
     a = ctypes.c_size_t(0)
     u = ctypes.c_size_t(0)
