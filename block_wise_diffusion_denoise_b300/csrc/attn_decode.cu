@@ -17,8 +17,8 @@
 // K is the A operand as staged (K-major, 128-byte swizzle); V^T is the same staged V tile
 // read M-major; Q and P^T are 16-row K-major tiles in shared memory.  Accumulators live in
 // tensor memory: two S^T buffers and O^T, 16 columns each.
-//  * Warps: 0 moves K and V tiles by TMA into two 3-stage rings, and each piece's 16 query
-//    rows; 1 issues the MMAs, the scores of tile j+1 ahead of the PV product of tile j;
+//  * Warps: 0 and 6 move K and V tiles by TMA into two 3-stage rings (0 also each piece's
+//    16 query rows); 1 issues the QK products and 7 the PV products;
 //    2-5 (one per TMEM lane quarter) run the softmax, one key per thread: the 16 scores of
 //    the key come from tensor memory, each head's maximum over the tile by a warp
 //    reduction and an exchange between the four warps in shared memory; the running
@@ -27,8 +27,11 @@
 //    P = 2^(s*c - m) goes as bf16 into a double-buffered P^T tile.  At the end of a piece
 //    thread r holds d lane r of O^T for the 16 heads and finishes their outputs.
 //  * Work split: the device-side split of the 128-row kernel (attn_work.cuh) with one CTA
-//    per group: whole segments, or stream-K pieces whose fp32 partials (O^T, m, l) are
-//    merged with log-sum-exp weights by the CTA that completes the segment's ticket.
+//    per group and a cost model of its own: whole segments, or stream-K pieces whose fp32
+//    partials (O^T, m, l) are merged with log-sum-exp weights by the CTA that completes
+//    the segment's ticket, after its own tiles.  Page ids are loaded a batch ahead of
+//    their use and Q is double-buffered, so that the producers never stall at a batch or
+//    piece boundary.
 //  * Every mbarrier wait is bounded; a wait that gives up records TT_ERR_DEVICE_TIMEOUT,
 //    and the CTA drains its copies and MMAs and exits.
 
@@ -47,26 +50,36 @@ using namespace sm100;
 
 constexpr int kDD = 128;                   // head dim
 constexpr int kG = 16;                     // query heads per KV head: the N of both products
-constexpr int kRing = 3;                   // K and V ring depth
+constexpr int kRingK = 3;                  // K ring depth (a K stage is free once QK has read it)
+constexpr int kRingV = 3;                  // V ring depth (a V stage is held until PV completes)
 constexpr int kTileHalf = 16384;           // one 64-column half of a 128-key tile (128 rows x 128 B)
 constexpr int kTile = 2 * kTileHalf;
 constexpr int kSmallHalf = kG * 128;       // one 64-column half of a 16-row tile (Q, P^T)
 constexpr int kSmall = 2 * kSmallHalf;
 constexpr int kSeqMaxD = 1024;             // sequences per launch (the host splits larger batches)
+constexpr int kMaxCtasD = 296;             // upper bound of the persistent grid
 constexpr int kOffKd = 0;
-constexpr int kOffVd = kOffKd + kRing * kTile;
-constexpr int kOffQd = kOffVd + kRing * kTile;
-constexpr int kOffPd = kOffQd + kSmall;                          // P^T [2 buffers]
+constexpr int kOffVd = kOffKd + kRingK * kTile;
+constexpr int kOffQd = kOffVd + kRingV * kTile;
+constexpr int kOffPd = kOffQd + 2 * kSmall;                      // Q [2 buffers], then P^T [2 buffers]
 constexpr int kOffPre = kOffPd + 2 * kSmall;                     // long long [kSeqMaxD + 1]
 constexpr int kOffLen = kOffPre + 8 * (kSeqMaxD + 1);            // int [kSeqMaxD]
-constexpr int kSmemD = kOffLen + 4 * kSeqMaxD + 1024;
+constexpr int kOffRange = kOffLen + 4 * kSeqMaxD;                // long long [kMaxCtasD + 1]
+constexpr int kSmemD = kOffRange + 8 * (kMaxCtasD + 1) + 1024;
 constexpr int kTmemColsD = 64;
 constexpr int kColSd = 0;                  // S^T[buf]: 16 fp32 columns each
 constexpr int kColOd = 32;                 // O^T: 16 fp32 columns
-constexpr int kMaxCtasD = 296;
 constexpr uint32_t kWaitLimitD = 1u << 20;
 constexpr float kRescaleD = 8.0f;          // log2 units
 constexpr int kSlotFloats = kG * kDD + 2 * kG;   // O^T as [16 heads][128 d], then m[16], l[16]
+
+// Work units of the split (attn_work.cuh): the token's own K/V tile is a full softmax
+// step but a 256-byte load, and a piece boundary costs little more than a tile: Q is a
+// 4 KB copy behind the K ring, and the epilogue of 16 heads x 128 d overlaps the next
+// piece's loads.
+struct DecCosts {
+    static constexpr int tile = 8, block = 6, seg = 8, split = 80, min_group = 64;
+};
 
 struct DecParams {
     const int32_t *page_table;
@@ -82,13 +95,13 @@ struct DecParams {
 };
 
 struct DBars {
-    uint64_t q_full, q_empty;
-    uint64_t k_full[kRing], k_empty[kRing], v_full[kRing], v_empty[kRing];
+    uint64_t q_full[2], q_empty[2];   // [piece parity]
+    uint64_t k_full[kRingK], k_empty[kRingK], v_full[kRingV], v_empty[kRingV];
     uint64_t s_full[2], s_empty[2];   // [tile parity]
     uint64_t p_full[2], p_free[2];    // [tile parity]
     uint64_t o_full, o_empty;
     uint64_t grp;                     // the four softmax warps among themselves
-    uint64_t done;                    // the issuer's last MMA has completed
+    uint64_t done[2];                 // each issuer's last MMA has completed
 };
 
 struct alignas(16) DShared {
@@ -141,7 +154,7 @@ __device__ __forceinline__ float pick(const float (&a)[kG], int i) {
     return v;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(256, 1)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vb,
                    const __grid_constant__ CUtensorMap tm_q, const DecParams p) {
@@ -153,12 +166,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int group = blockIdx.x;
     DBars &bar = sh.bar;
     if (threadIdx.x == 0) {
-        mbar_init(&bar.q_full, 1);
-        mbar_init(&bar.q_empty, 1);
-        for (int s = 0; s < kRing; ++s) {
-            mbar_init(&bar.k_full[s], 1); mbar_init(&bar.k_empty[s], 1);
-            mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1);
-        }
+        for (int s = 0; s < 2; ++s) { mbar_init(&bar.q_full[s], 1); mbar_init(&bar.q_empty[s], 1); }
+        for (int s = 0; s < kRingK; ++s) { mbar_init(&bar.k_full[s], 1); mbar_init(&bar.k_empty[s], 1); }
+        for (int s = 0; s < kRingV; ++s) { mbar_init(&bar.v_full[s], 1); mbar_init(&bar.v_empty[s], 1); }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar.s_full[s], 1); mbar_init(&bar.s_empty[s], 4);
             mbar_init(&bar.p_full[s], 4); mbar_init(&bar.p_free[s], 1);
@@ -166,7 +176,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         mbar_init(&bar.o_full, 1);
         mbar_init(&bar.o_empty, 4);
         mbar_init(&bar.grp, 4);
-        mbar_init(&bar.done, 1);
+        mbar_init(&bar.done[0], 1);
+        mbar_init(&bar.done[1], 1);
         fence_mbar_init();
         sh.abort = 0;
         prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_kb); prefetch_tmap(&tm_vb);
@@ -191,7 +202,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         if (lane == 0) seq_pre[0] = 0;
         for (int base = 0; base < p.B; base += 32) {
             const int i = base + lane;
-            long long v = (i < p.B) ? (long long)seq_cost(seq_len[i], p.Hkv) : 0;
+            long long v = (i < p.B) ? (long long)seq_cost<DecCosts>(seq_len[i], p.Hkv) : 0;
             if (i < p.B) mlen = max(mlen, seq_len[i]);
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -208,87 +219,110 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    WorkIter it;
+    WorkIter<DecCosts> it;
     it.init(p, group, seq_pre, seq_len, sh.max_len);
 
-    if (warp == 0) {
-        // ================================================================ TMA producer
-        // Per piece the 16 query rows of its KV head; per tile the K tile into the K ring and
-        // the V tile into the V ring (the two pages of a context tile, or the token's own key
-        // and value for the block tile).  Page ids are fetched 32 at a time, one per lane.
-        Piece pc;
+    if (warp == 0 || warp == 6) {
+        // ================================================================ TMA producers
+        // Warp 0 loads K (and each piece's 16 query rows), warp 6 loads V, so that a K copy
+        // never waits behind the release of a V stage (V is held until its PV product has
+        // completed, K only until QK has read it).  Each whole warp walks the work (page
+        // ids are fetched 32 at a time, one per lane); lane 0 issues the copies: the two
+        // pages of a context tile, or the token's own key / value for the block tile.
+        const bool is_v = warp == 6;
+        const int nst = is_v ? kRingV : kRingK;
+        uint64_t *full = is_v ? bar.v_full : bar.k_full;
+        uint64_t *empty = is_v ? bar.v_empty : bar.k_empty;
+        const CUtensorMap *pool = is_v ? &tm_v : &tm_k;
+        const CUtensorMap *blk = is_v ? &tm_vb : &tm_kb;
+        unsigned char *ring = sm + (is_v ? kOffVd : kOffKd);
+        const uint64_t pol = policy_evict_first();
+        // Page ids are loaded one batch (16 tiles, one page per lane) ahead of their use --
+        // the next batch of the piece, or the first of the next piece, which a second
+        // iterator running one piece ahead names -- so that no copy waits on a page-table
+        // load.
+        WorkIter<DecCosts> ahead = it;
+        Piece pc, pn;
+        bool have = ahead.next(p, pc);
+        bool have_n = have && ahead.next(p, pn);
+        int cur = have ? page_id(p, pc, 2 * pc.first + lane) : 0, nxt = 0;
         int t = 0, qi = 0;
         bool ok = true;
-        while (ok && it.next(p, pc)) {
-            if (!dwait(sh, &bar.q_empty, ((uint32_t)qi & 1) ^ 1, p.dev_err)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bar.q_full, kSmall);
-                const int row = pc.b * p.Hq + pc.g * kG;
-                tma_load_3d(sm + kOffQd, &tm_q, &bar.q_full, 0, row, 0);
-                tma_load_3d(sm + kOffQd + kSmallHalf, &tm_q, &bar.q_full, 64, row, 0);
+        while (ok && have) {
+            if (!is_v) {
+                // Q of the piece into its buffer (two buffers: the next piece's Q does not
+                // wait for the last QK product of this one)
+                const int qb = qi & 1;
+                if (!dwait(sh, &bar.q_empty[qb], (((uint32_t)qi >> 1) & 1) ^ 1, p.dev_err)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar.q_full[qb], kSmall);
+                    const int row = pc.b * p.Hq + pc.g * kG;
+                    tma_load_3d(sm + kOffQd + qb * kSmall, &tm_q, &bar.q_full[qb], 0, row, 0);
+                    tma_load_3d(sm + kOffQd + qb * kSmall + kSmallHalf, &tm_q, &bar.q_full[qb], 64, row, 0);
+                }
+                ++qi;
             }
-            ++qi;
-            int my_page = 0;
             for (int i = pc.first; i < pc.last; ++i, ++t) {
                 const int rel = i - pc.first;
-                if ((rel & 15) == 0) my_page = page_id(p, pc, 2 * i + lane);
-                const int page0 = __shfl_sync(0xffffffffu, my_page, (2 * rel) & 31);
-                const int page1 = __shfl_sync(0xffffffffu, my_page, (2 * rel + 1) & 31);
+                if ((rel & 15) == 0) {
+                    if (rel > 0) cur = nxt;
+                    if (i + 16 < pc.last) nxt = page_id(p, pc, 2 * (i + 16) + lane);
+                    else if (have_n) nxt = page_id(p, pn, 2 * pn.first + lane);
+                }
+                const int page0 = __shfl_sync(0xffffffffu, cur, (2 * rel) & 31);
+                const int page1 = __shfl_sync(0xffffffffu, cur, (2 * rel + 1) & 31);
                 const bool ctx = i < pc.ntc;
                 const bool two = ctx && tile_valid(pc, i, 1) > kPage;
-                const int st = t % kRing;
-                const uint32_t par = ((uint32_t)(t / kRing) & 1) ^ 1;
-                for (int kv = 0; kv < 2; ++kv) {
-                    uint64_t *empty = kv ? &bar.v_empty[st] : &bar.k_empty[st];
-                    uint64_t *full = kv ? &bar.v_full[st] : &bar.k_full[st];
-                    const CUtensorMap *pool = kv ? &tm_v : &tm_k;
-                    const CUtensorMap *blk = kv ? &tm_vb : &tm_kb;
-                    unsigned char *dst = sm + (kv ? kOffVd : kOffKd) + st * kTile;
-                    if (!dwait(sh, empty, par, p.dev_err)) { ok = false; break; }
-                    if (lane == 0) {
-                        if (ctx) {
-                            mbar_arrive_expect_tx(full, two ? 4 * 8192u : 2 * 8192u);
-                            tma_load_4d(dst, pool, full, 0, 0, pc.g, page0);
-                            tma_load_4d(dst + kTileHalf, pool, full, 64, 0, pc.g, page0);
-                            if (two) {
-                                tma_load_4d(dst + 8192, pool, full, 0, 0, pc.g, page1);
-                                tma_load_4d(dst + kTileHalf + 8192, pool, full, 64, 0, pc.g, page1);
-                            }
-                        } else {
-                            mbar_arrive_expect_tx(full, 2 * 128u);
-                            tma_load_3d(dst, blk, full, 0, pc.g, pc.b);
-                            tma_load_3d(dst + kTileHalf, blk, full, 64, pc.g, pc.b);
+                const int st = t % nst;
+                if (!dwait(sh, &empty[st], ((uint32_t)(t / nst) & 1) ^ 1, p.dev_err)) { ok = false; break; }
+                unsigned char *dst = ring + st * kTile;
+                if (lane == 0) {
+                    if (ctx) {
+                        // the pages are read once per launch: first out of L2
+                        mbar_arrive_expect_tx(&full[st], two ? 4 * 8192u : 2 * 8192u);
+                        tma_load_4d_hint(dst, pool, &full[st], 0, 0, pc.g, page0, pol);
+                        tma_load_4d_hint(dst + kTileHalf, pool, &full[st], 64, 0, pc.g, page0, pol);
+                        if (two) {
+                            tma_load_4d_hint(dst + 8192, pool, &full[st], 0, 0, pc.g, page1, pol);
+                            tma_load_4d_hint(dst + kTileHalf + 8192, pool, &full[st], 64, 0, pc.g, page1, pol);
                         }
+                    } else {
+                        mbar_arrive_expect_tx(&full[st], 2 * 128u);
+                        tma_load_3d(dst, blk, &full[st], 0, pc.g, pc.b);
+                        tma_load_3d(dst + kTileHalf, blk, &full[st], 64, pc.g, pc.b);
                     }
-                    __syncwarp();
                 }
-                if (!ok) break;
+                __syncwarp();
             }
+            // the last batch of a piece always prefetched the first batch of the next one
+            cur = nxt;
+            pc = pn;
+            have = have_n;
+            have_n = have && ahead.next(p, pn);
         }
-        // Drain: every copy issued must land before the CTA may exit.  (After an abort
-        // between the K and the V copy of a tile, the V wait below runs out: bounded.)
-        for (int k = 1; k <= kRing && t - k >= 0; ++k) {
-            mbar_wait(&bar.k_full[(t - k) % kRing], (uint32_t)((t - k) / kRing) & 1, kWaitLimitD);
-            mbar_wait(&bar.v_full[(t - k) % kRing], (uint32_t)((t - k) / kRing) & 1, kWaitLimitD);
-        }
+        // Drain: every copy issued must land before the CTA may exit.  The last copy into a
+        // stage completes that stage's latest phase.
+        for (int k = 1; k <= nst && t - k >= 0; ++k)
+            mbar_wait(&full[(t - k) % nst], (uint32_t)((t - k) / nst) & 1, kWaitLimitD);
         __syncwarp();
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
-        // The scores of tile j+1 are issued before the PV product of tile j, so that the
-        // softmax of one tile overlaps the QK product of the next.
+    } else if (warp == 1 || warp == 7) {
+        // ================================================================ MMA issuers
+        // Warp 1 issues the QK products, warp 7 the PV products.  A commit tracks the MMAs
+        // of the thread that issued them, so a V stage (and the P^T buffer) is released as
+        // soon as its own PV product has completed, whatever QK products are queued.
         const uint32_t idesc_qk = idesc_bf16_f32(128, kG, false, false);
         const uint32_t idesc_pv = idesc_bf16_f32(128, kG, true, false);
-        const uint32_t qb = smem_u32(sm + kOffQd);
         Piece pc;
         int t0 = 0, qi = 0, pi = 0;
         bool ok = true;
-        // S^T[tt & 1] = K_tile . Q^T for tile tt
-        auto issue_qk = [&](int tt, bool last) -> bool {
-            const int st = tt % kRing;
-            if (!dwait(sh, &bar.k_full[st], (uint32_t)(tt / kRing) & 1, p.dev_err)) return false;
+        // S^T[tt & 1] = K_tile . Q^T for tile tt, with the piece's Q in buffer qbuf
+        auto issue_qk = [&](int tt, int qbuf, bool last) -> bool {
+            const int st = tt % kRingK;
+            if (!dwait(sh, &bar.k_full[st], (uint32_t)(tt / kRingK) & 1, p.dev_err)) return false;
             if (!dwait(sh, &bar.s_empty[tt & 1], (((uint32_t)tt >> 1) & 1) ^ 1, p.dev_err)) return false;
             tc_fence_after();
             const uint32_t kbase = smem_u32(sm + kOffKd + st * kTile);
+            const uint32_t qb = smem_u32(sm + kOffQd + qbuf * kSmall);
             const uint32_t dcol = tmem + kColSd + 16 * (tt & 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {   // 16 head dimensions per step
@@ -300,7 +334,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             if (elect_one()) {
                 mma_commit(&bar.s_full[tt & 1]);
                 mma_commit(&bar.k_empty[st]);
-                if (last) mma_commit(&bar.q_empty);
+                if (last) mma_commit(&bar.q_empty[qbuf]);
             }
             __syncwarp();
             return true;
@@ -308,9 +342,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         // O^T += V_tile^T . P^T for tile tt (j-th of its piece); rows of the V tile past the
         // valid keys are zeroed first (their P is 0, but stale bits could hold a NaN)
         auto issue_pv = [&](int tt, int j, int valid, bool last) -> bool {
-            const int st = tt % kRing;
+            const int st = tt % kRingV;
             const int nk = (valid + 15) & ~15;
-            if (!dwait(sh, &bar.v_full[st], (uint32_t)(tt / kRing) & 1, p.dev_err)) return false;
+            if (!dwait(sh, &bar.v_full[st], (uint32_t)(tt / kRingV) & 1, p.dev_err)) return false;
             unsigned char *vp = sm + kOffVd + st * kTile;
             if (valid < nk) {
                 const int words = (nk - valid) * 8;   // 16-byte words per half
@@ -341,18 +375,20 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             return true;
         };
         while (ok && it.next(p, pc)) {
-            if (!dwait(sh, &bar.q_full, (uint32_t)qi & 1, p.dev_err)) break;
-            ++qi;
             const int ntiles = pc.last - pc.first;
-            ok = issue_qk(t0, ntiles == 1);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                if (j + 1 < ntiles) ok = issue_qk(t0 + j + 1, j + 2 == ntiles);
-                if (ok) ok = issue_pv(t0 + j, j, tile_valid(pc, pc.first + j, 1), j + 1 == ntiles);
+            if (warp == 1) {
+                const int qbuf = qi & 1;
+                if (!dwait(sh, &bar.q_full[qbuf], ((uint32_t)qi >> 1) & 1, p.dev_err)) break;
+                ++qi;
+                for (int j = 0; ok && j < ntiles; ++j) ok = issue_qk(t0 + j, qbuf, j + 1 == ntiles);
+            } else {
+                for (int j = 0; ok && j < ntiles; ++j)
+                    ok = issue_pv(t0 + j, j, tile_valid(pc, pc.first + j, 1), j + 1 == ntiles);
             }
             t0 += ntiles;
             ++pi;
         }
-        if (elect_one()) mma_commit(&bar.done);
+        if (elect_one()) mma_commit(&bar.done[warp == 1 ? 0 : 1]);
         __syncwarp();
     } else {
         // ================================================================ softmax / epilogue
@@ -363,7 +399,66 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const uint32_t lane_off = (uint32_t)(32 * wq) << 16;
         const float c2 = p.scale_log2;
         const int pt_half = r >> 6, pt_chunk = (r & 63) >> 3, pt_within = (r & 7) * 2;
-        Piece pc;
+        // Merge every piece of a split segment in group order (d lane r of each head) and
+        // leave its ticket at zero for the next launch.
+        // lo[c] of every group (for the merges), filled while the first tiles load
+        long long *range_tab = reinterpret_cast<long long *>(sm + kOffRange);
+        for (int c = r; c <= it.NG; c += 128) range_tab[c] = range_lo(c, it.U, it.NG);
+        auto merge = [&](const Piece &q) {
+            const int n = it.NG;
+            const int c_first = owner_tab(q.X + DecCosts::seg, range_tab, n);
+            const int c_last = owner_tab(q.X + DecCosts::seg + (long long)DecCosts::tile * q.ntc, range_tab, n);
+            float M[kG], Ls[kG], acc[kG];
+#pragma unroll
+            for (int h = 0; h < kG; ++h) { M[h] = -INFINITY; Ls[h] = 0.f; acc[h] = 0.f; }
+            // up to four pieces per round, every load of a round in flight at once: lane L
+            // loads the maximum (L < 16) or the sum (L >= 16) of head L % 16, and every thread
+            // its d lane of the 16 heads
+            for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+                bool u[4];
+                float ml[4], o[4][kG];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    u[k] = c0 + k <= c_last && owns_tile_tab<DecCosts>(c0 + k, q.X, q.ntc, range_tab);
+                    const float *sl = p.part + (long long)(c0 + k + q.sg) * kSlotFloats;
+                    ml[k] = u[k] ? __ldcg(sl + kG * kDD + lane) : (lane < kG ? -INFINITY : 0.f);
+#pragma unroll
+                    for (int h = 0; h < kG; ++h) o[k][h] = u[k] ? __ldcg(sl + h * kDD + r) : 0.f;
+                }
+#pragma unroll
+                for (int h = 0; h < kG; ++h) {
+                    float mk[4], lk[4];
+                    float Mn = M[h];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        mk[k] = __shfl_sync(0xffffffffu, ml[k], h);
+                        lk[k] = __shfl_sync(0xffffffffu, ml[k], kG + h);
+                        Mn = fmaxf(Mn, mk[k]);
+                    }
+                    if (Mn == -INFINITY) continue;   // no piece yet for this head
+                    const float a = fast_exp2(M[h] - Mn);
+                    float ls = Ls[h] * a, ac = acc[h] * a;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float w = fast_exp2(mk[k] - Mn);
+                        ls += lk[k] * w;
+                        ac += o[k][h] * w;
+                    }
+                    Ls[h] = ls;
+                    acc[h] = ac;
+                    M[h] = Mn;
+                }
+            }
+            const int hq0 = q.g * kG;
+            uint16_t *out = p.out + ((size_t)q.b * p.Hq + hq0) * kDD + r;
+#pragma unroll
+            for (int h = 0; h < kG; ++h) out[h * kDD] = to_bf16(acc[h] / Ls[h]);
+            if (p.lse && r < kG)
+                p.lse[(size_t)q.b * p.Hq + hq0 + r] = (pick(M, r) + __log2f(pick(Ls, r))) * kLn2;
+            if (r == 0) p.tickets[q.sg] = 0;
+        };
+        Piece pc, pend0, pend1;           // the split pieces of this CTA (at most two)
+        int npend = 0, last0 = 0, last1 = 0;  // (last*: thread r == 0 only)
         int t = 0, pi = 0, k_grp = 0;
         bool ok = true;
         while (ok && it.next(p, pc)) {
@@ -481,48 +576,34 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     __stcg(slot + kG * kDD + r, pick(m, r));
                     __stcg(slot + kG * kDD + kG + r, pick(l, r));
                 }
-                // one thread publishes the piece: the meeting orders every thread's stores
-                // before its release, the acquire half orders the merge's loads after it
+                // One thread publishes the piece: the meeting orders every thread's stores
+                // before its release.  The add returns at once (release only), so the
+                // pipeline does not wait for it; whether this piece completed the segment is
+                // read at the end, where the last one acquires (fence) and merges -- after
+                // this CTA's own tiles (at most two split pieces: only the first and the last
+                // piece of a CTA's range can be split).
                 if (!dgroup_sync(sh, k_grp, p.dev_err)) { ok = false; break; }
-                unsigned *ticket = p.tickets + pc.sg;
                 if (r == 0) {
                     const unsigned n_here = (unsigned)(pc.last - pc.first);
-                    const unsigned before = atom_add_acq_rel_gpu(ticket, n_here);
-                    sh.last = (before + n_here == (unsigned)(pc.ntc + 1));
+                    const unsigned before = atom_add_release_gpu(p.tickets + pc.sg, n_here);
+                    const int done = (before + n_here == (unsigned)(pc.ntc + 1)) ? 1 : 0;
+                    if (npend == 0) last0 = done; else last1 = done;
                 }
-                if (!dgroup_sync(sh, k_grp, p.dev_err)) { ok = false; break; }
-                if (sh.last) {
-                    // merge every piece of the segment in group order (d lane r of each head)
-                    const long long U = it.U;
-                    const int n = it.NG;
-                    const int c_first = owner(pc.X + kCostSeg, U, n);
-                    const int c_last = owner(pc.X + kCostSeg + (long long)kCostTile * pc.ntc, U, n);
-                    float M[kG], Ls[kG], acc[kG];
-#pragma unroll
-                    for (int h = 0; h < kG; ++h) { M[h] = -INFINITY; Ls[h] = 0.f; acc[h] = 0.f; }
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        if (!owns_tile(cc, pc.X, pc.ntc, U, n)) continue;
-                        const float *sl = p.part + (long long)(cc + pc.sg) * kSlotFloats;
-#pragma unroll
-                        for (int h = 0; h < kG; ++h) {
-                            const float ov = __ldcg(sl + h * kDD + r);
-                            const float mc = __ldcg(sl + kG * kDD + h);
-                            const float lc = __ldcg(sl + kG * kDD + kG + h);
-                            const float Mn = fmaxf(M[h], mc);
-                            const float a = fast_exp2(M[h] - Mn), w = fast_exp2(mc - Mn);
-                            Ls[h] = Ls[h] * a + lc * w;
-                            acc[h] = acc[h] * a + ov * w;
-                            M[h] = Mn;
-                        }
-                    }
-#pragma unroll
-                    for (int h = 0; h < kG; ++h) out[h * kDD] = to_bf16(acc[h] / Ls[h]);
-                    if (p.lse && r < kG)
-                        p.lse[(size_t)pc.b * p.Hq + hq0 + r] = (pick(M, r) + __log2f(pick(Ls, r))) * kLn2;
-                    if (r == 0) *ticket = 0;   // ready for the next launch
-                }
+                if (npend == 0) pend0 = pc; else pend1 = pc;
+                ++npend;
             }
             ++pi;
+        }
+        if (ok && npend > 0) {
+            if (r == 0) {
+                if (last0 | last1) fence_acq_rel_gpu();
+                sh.last = last0 | (last1 << 1);
+            }
+            if (dgroup_sync(sh, k_grp, p.dev_err)) {
+                const int f = sh.last;
+                if (f & 1) merge(pend0);
+                if (npend > 1 && (f & 2)) merge(pend1);
+            }
         }
     }
 
@@ -531,7 +612,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        mbar_wait(&bar.done, 0, kWaitLimitD);
+        mbar_wait(&bar.done[0], 0, kWaitLimitD);
+        mbar_wait(&bar.done[1], 0, kWaitLimitD);
         tmem_dealloc(tmem, kTmemColsD);
     }
 }
@@ -597,7 +679,7 @@ tt_status launch_attn_decode(const AttnArgs &a) {
         p.tickets = static_cast<unsigned *>(a.ws);
         p.part = reinterpret_cast<float *>(static_cast<char *>(a.ws) + align_up(nseg * sizeof(unsigned), 256));
         p.dev_err = a.dev_err;
-        attn_decode_kernel<<<n, 192, kSmemD, a.stream>>>(mk, mv, mkb, mvb, mq, p);
+        attn_decode_kernel<<<n, 256, kSmemD, a.stream>>>(mk, mv, mkb, mvb, mq, p);
         if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
     }
     return TT_OK;

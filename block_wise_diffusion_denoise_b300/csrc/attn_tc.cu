@@ -294,7 +294,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (lane == 0) seq_pre[0] = 0;
         for (int base = 0; base < p.B; base += 32) {
             const int i = base + lane;
-            long long v = (i < p.B) ? (long long)seq_cost(seq_len[i], p.Hkv) : 0;
+            long long v = (i < p.B) ? (long long)seq_cost<TcCosts>(seq_len[i], p.Hkv) : 0;
             if (i < p.B) mlen = max(mlen, seq_len[i]);
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -312,7 +312,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    WorkIter it;
+    WorkIter<TcCosts> it;
     it.init(p, group, seq_pre, seq_len, sh.max_len);
     const int S = p.S, G = p.G;
 
@@ -693,14 +693,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                     // output values are loaded together).
                     const long long U = it.U;
                     const int n = it.NG;
-                    const int c_first = owner(pc.X + kCostSeg, U, n);
-                    const int c_last = owner(pc.X + kCostSeg + (long long)kCostTile * pc.ntc, U, n);
+                    const int c_first = first_owner<TcCosts>(pc.X, U, n);
+                    const int c_last = last_owner<TcCosts>(pc.X, pc.ntc, U, n);
                     float M = -INFINITY, Lsum = 0.f;
                     float acc[64];
 #pragma unroll
                     for (int d = 0; d < 64; ++d) acc[d] = 0.f;
                     for (int c = c_first; c <= c_last; ++c) {
-                        if (!owns_tile(c, pc.X, pc.ntc, U, n)) continue;
+                        if (!owns_tile<TcCosts>(c, pc.X, pc.ntc, U, n)) continue;
                         const float *sl = p.part + (long long)(c + pc.sg) * p.slot_floats;
                         const float4 *orw = reinterpret_cast<const float4 *>(sl) + (size_t)16 * h * p.rows + r;
                         float4 v[16];

@@ -3,11 +3,11 @@
 //
 // A segment is one (sequence b, KV head g): the query rows that share every key of that
 // head.  Its keys are ceil(L_b / kTileKeys) context tiles of two pages each, then one tile
-// of the block's own keys.  Work is counted in units -- kCostSeg per segment for what a
-// piece boundary costs, kCostTile per context tile, kCostBlock for the block tile -- and
-// cut into one range per CTA group: whole segments when every group can take one and
-// splitting would not pay, otherwise equal unit ranges (stream-K), so ragged and long
-// contexts balance with the lengths known only on the device.
+// of the block's own keys.  Work is counted in units -- a charge per segment for what a
+// piece boundary costs, one per context tile, one for the block tile (a cost model per
+// kernel) -- and cut into one range per CTA group: whole segments when every group can
+// take one and splitting would not pay, otherwise equal unit ranges (stream-K), so ragged
+// and long contexts balance with the lengths known only on the device.
 #pragma once
 
 #include <cuda.h>
@@ -23,23 +23,27 @@ namespace {
 
 constexpr int kPage = 64;                // tokens per page
 constexpr int kTileKeys = 128;           // keys per context tile (two pages)
-// Work units of the stream-K split: a context tile costs kCostTile, the block tile
-// kCostBlock (its MMAs are short but its softmax is a full tile's), and every segment
-// carries kCostSeg up front for what a piece boundary costs (Q load, pipeline refill,
-// epilogue and, for split segments, the merge).
-constexpr int kCostTile = 8, kCostBlock = 6, kCostSeg = 24;
-// Splitting a segment between groups costs about this many units more than it saves
-// (a second piece boundary, the partial write and the merge): when every group can take
-// a whole segment and the longest one is within this margin of the even split, each
-// group takes one whole segment instead.
-constexpr int kCostSplit = 80;
-// A stream-K group gets at least this many units (eight tiles) of work.
-constexpr int kMinGroupUnits = 64;
+
+// Work units of the stream-K split, one cost model per kernel: a context tile costs
+// `tile`, the block tile `block`, and every segment carries `seg` up front for what a
+// piece boundary costs (Q load, pipeline refill, epilogue and, for split segments, the
+// merge).  When every group can take a whole segment and the longest one is within
+// `split` units of the even share (splitting would cost about that much more than it
+// saves: a second boundary, the partial write and the merge), each group takes one whole
+// segment; a stream-K group gets at least `min_group` units.
+//
+// The 128-row kernel: its block tile's MMAs are short but its softmax is a full tile's,
+// and a boundary costs about three tiles (the Q load into tensor memory and the epilogue
+// of 128 rows x 128 columns).
+struct TcCosts {
+    static constexpr int tile = 8, block = 6, seg = 24, split = 80, min_group = 64;
+};
 
 // ------------------------------------------------------------------ work partition
 
+template <class C>
 __device__ __forceinline__ int seq_cost(int L, int Hkv) {
-    return Hkv * (kCostSeg + kCostTile * ((L + kTileKeys - 1) / kTileKeys) + kCostBlock);
+    return Hkv * (C::seg + C::tile * ((L + kTileKeys - 1) / kTileKeys) + C::block);
 }
 
 struct Piece {
@@ -51,11 +55,12 @@ struct Piece {
 };
 
 // Walks the pieces of one CTA group's cost range [lo, hi).  Tile i of a segment that
-// starts at unit X starts at unit X + kCostSeg + kCostTile * i (the block tile is i = ntc).
+// starts at unit X starts at unit X + C::seg + C::tile * i (the block tile is i = ntc).
+template <class C>
 struct WorkIter {
     long long U, lo, hi, X;
     int NG;                 // groups that share the work (the stream-K split's divisor)
-    int b, g, L, ntc, C;
+    int b, g, L, ntc, cost;
     int B, Hkv;
     const long long *pre;   // shared: prefix sums of the sequences' work units
     const int *lens;        // shared: clamped context lengths
@@ -65,21 +70,21 @@ struct WorkIter {
         B = p.B; Hkv = p.Hkv; pre = pre_; lens = lens_;
         U = pre[B];
         const long long nseg = (long long)B * Hkv;
-        const long long max_seg = seq_cost(max_len, 1);
+        const long long max_seg = seq_cost<C>(max_len, 1);
         NG = p.n_groups;
-        if (nseg <= p.n_groups && max_seg <= U / p.n_groups + kCostSplit) {
+        if (nseg <= p.n_groups && max_seg <= U / p.n_groups + C::split) {
             // one whole segment per group: the range of segment `group` exactly
             if (group < nseg) {
                 const int sb = (int)(group / Hkv), sg = (int)(group % Hkv);
-                lo = pre[sb] + (long long)sg * seq_cost(lens[sb], 1);
-                hi = lo + seq_cost(lens[sb], 1);
+                lo = pre[sb] + (long long)sg * seq_cost<C>(lens[sb], 1);
+                hi = lo + seq_cost<C>(lens[sb], 1);
             } else {
                 lo = hi = U;
             }
         } else {
-            // stream-K over at most U / kMinGroupUnits groups, so that a small batch is not
+            // stream-K over at most U / C::min_group groups, so that a small batch is not
             // cut into one-tile pieces whose merges would cost more than the tiles
-            const long long ng = U / kMinGroupUnits;
+            const long long ng = U / C::min_group;
             NG = (int)(ng < 1 ? 1 : (ng < p.n_groups ? ng : p.n_groups));
             if (group < NG) {
                 lo = (long long)group * U / NG;
@@ -102,15 +107,15 @@ struct WorkIter {
         if (b < B) {
             L = lens[b];
             ntc = (L + kTileKeys - 1) / kTileKeys;
-            C = kCostSeg + kCostTile * ntc + kCostBlock;
+            cost = C::seg + C::tile * ntc + C::block;
         }
     }
     template <class P>
     __device__ bool next(const P &, Piece &pc) {
         while (b < B && X < hi) {
-            const long long T0 = X + kCostSeg;   // unit of tile 0
-            const long long first = (lo > T0) ? (lo - T0 + kCostTile - 1) / kCostTile : 0;
-            long long last = (hi > T0) ? (hi - T0 + kCostTile - 1) / kCostTile : 0;
+            const long long T0 = X + C::seg;   // unit of tile 0
+            const long long first = (lo > T0) ? (lo - T0 + C::tile - 1) / C::tile : 0;
+            long long last = (hi > T0) ? (hi - T0 + C::tile - 1) / C::tile : 0;
             if (last > ntc + 1) last = ntc + 1;
             const bool have = first < last;
             if (have) {
@@ -118,7 +123,7 @@ struct WorkIter {
                 pc.first = (int)first; pc.last = (int)last; pc.X = X;
                 pc.whole = (first == 0 && last == ntc + 1);
             }
-            X += C;
+            X += cost;
             if (++g == Hkv) { g = 0; ++b; load(); }
             if (have) return true;
         }
@@ -137,11 +142,38 @@ __device__ __forceinline__ int owner(long long u, long long U, int n) {
 }
 
 // Does group c own at least one tile of the segment starting at unit X with ntc context tiles?
+template <class C>
 __device__ __forceinline__ bool owns_tile(int c, long long X, int ntc, long long U, int n) {
     const long long lo_c = range_lo(c, U, n), hi_c = range_lo(c + 1, U, n);
-    const long long T0 = X + kCostSeg;
-    const long long i0 = (lo_c > T0) ? (lo_c - T0 + kCostTile - 1) / kCostTile : 0;
-    return i0 <= ntc && T0 + kCostTile * i0 < hi_c;
+    const long long T0 = X + C::seg;
+    const long long i0 = (lo_c > T0) ? (lo_c - T0 + C::tile - 1) / C::tile : 0;
+    return i0 <= ntc && T0 + C::tile * i0 < hi_c;
+}
+
+// The same questions answered from a table lo[c] = range_lo(c) for c = 0..n (filled once
+// per launch), without 64-bit divisions.
+__device__ __forceinline__ int owner_tab(long long u, const long long *lo, int n) {
+    int a = 0, z = n - 1;   // the last c with lo[c] <= u
+    while (a < z) {
+        const int mid = (a + z + 1) >> 1;
+        if (lo[mid] <= u) a = mid; else z = mid - 1;
+    }
+    return a;
+}
+template <class C>
+__device__ __forceinline__ bool owns_tile_tab(int c, long long X, int ntc, const long long *lo) {
+    const long long lo_c = lo[c], hi_c = lo[c + 1];
+    const long long T0 = X + C::seg;
+    const long long i0 = (lo_c > T0) ? (lo_c - T0 + C::tile - 1) / C::tile : 0;
+    return i0 <= ntc && T0 + C::tile * i0 < hi_c;
+}
+
+// The groups that own the first and the last tile of the segment starting at unit X.
+template <class C>
+__device__ __forceinline__ int first_owner(long long X, long long U, int n) { return owner(X + C::seg, U, n); }
+template <class C>
+__device__ __forceinline__ int last_owner(long long X, int ntc, long long U, int n) {
+    return owner(X + C::seg + (long long)C::tile * ntc, U, n);
 }
 
 // Physical page of logical page pg of the piece's sequence (0 past the context; an id

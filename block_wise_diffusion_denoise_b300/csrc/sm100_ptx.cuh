@@ -121,6 +121,23 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
+// An L2 policy that evicts first what it tags (data read exactly once).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_4d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
 // Bring a 4-D box into L2 ahead of its load (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int c0, int c1, int c2, int c3) {
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
@@ -294,6 +311,20 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *ptr, unsigned
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
     return old;
 }
+
+// Fetch-and-add with release semantics at GPU scope: the caller's (and, after a CTA
+// barrier, its block's) earlier writes are visible to whoever acquires the value; later
+// operations of the caller are not held back by it.
+__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned *ptr, unsigned v) {
+    unsigned old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
+// Acquire half of a synchronisation through an earlier read (the value an atomic returned):
+// with the fence, the writes released before that value are visible to the caller's later
+// operations.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 }  // namespace sm100
 }  // namespace tt
