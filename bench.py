@@ -60,6 +60,7 @@ PROFILED = {   # kernel -> (summary under profiles/, the sources its counters we
     "attention": ("attention_ctx8k.md", ("attn_tc.cu", "sm100_ptx.cuh", "tt_common.cuh")),
     "unmask": ("unmask_ctx8k.md", ("unmask.cu", "vocab_stream.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
     "masked_nll": ("masked_nll_ctx8k.md", ("masked_nll.cu", "vocab_stream.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
+    "decode": ("decode_attention_ctx8k.md", ("attn_decode.cu", "attn_work.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
 }
 
 
@@ -415,6 +416,17 @@ def run_ours(a, cfg):
         api.tt_masked_nll(c["lg"], nll_targets, nll_masked, nll=nll_out, nll_sum=nll_sum, count=nll_cnt, ws=nll_ws,
                           dev_err=err, stream=stream)
 
+    # one decoding position (S = 1) per sequence on the same caches: the first block position's
+    # q / k / v (the decode kernel; every query head of a KV head in one pass over the context)
+    dec = [{"q": c["q"][:, :1].contiguous(), "kb": c["kb"][:, :1].contiguous(), "vb": c["vb"][:, :1].contiguous(),
+            "out": torch.empty_like(c["q"][:, :1])} for c in copies]
+    dec_ws = api.workspace(api.tt_denoise_attn_workspace_size(cfg.B, 1, cfg.Hq, cfg.Hkv, cfg.D, tdt), dev)
+
+    def decode_only(i, stream=None):
+        c, d = copies[i % n_copies], dec[i % n_copies]
+        api.tt_denoise_attn(c["cache"], d["q"], d["kb"], d["vb"], out=d["out"], sm_scale=scale, ws=dec_ws,
+                            dev_err=err, stream=stream)
+
     def barrier():
         if world > 1:
             dist.barrier()
@@ -496,6 +508,10 @@ def run_ours(a, cfg):
     ctx_attn_ms = timed(ctx_attn_only, 0, k_ker, use_graph) / k_ker
     # the training-side loss over the same logits (not part of the denoise step)
     nll_ms = timed(nll_only, 0, k_ker, use_graph) / k_ker
+    # one autoregressive decoding step's attention on the same contexts (S = 1)
+    dec_ms = timed(decode_only, 0, k_ker, use_graph) / k_ker
+    # positions the timed denoise steps committed (the first step of a fresh block)
+    commits = float(committed[a.warmup:].sum().item()) / a.steps
     # block sizes S = 32, 64, 128 on the same contexts (the attention alone)
     s_var = {}
     if a.s_variants:
@@ -583,6 +599,7 @@ def run_ours(a, cfg):
         src = "of measured" if peaks else "of fallback"
         ab, af = attn_bytes(cfg, lens), attn_flops(cfg, lens)
         ub = unmask_bytes(cfg, cfg.B * cfg.S)
+        db = attn_bytes(cfg.replace(S=1), lens)
         attn_gbs = ab / (attn_ms * 1e-3) / 1e9
         attn_tfs = af / (attn_ms * 1e-3) / 1e12
         unm_gbs = ub / (unmask_ms * 1e-3) / 1e9
@@ -617,7 +634,21 @@ def run_ours(a, cfg):
                     "roofline_us": ub / (hbm * 1e9) * 1e6,
                     "note": "tt_masked_nll over the step's logits with every position masked; timed separately, "
                             "not in the step"},
+                "decode_attention": {
+                    "us": dec_ms * 1e3, "gbs": db / (dec_ms * 1e-3) / 1e9, "hbm_frac": db / (dec_ms * 1e-3) / 1e9 / hbm,
+                    "roofline_us": db / (hbm * 1e9) * 1e6, "traffic": profiled_traffic("decode", cfg.name),
+                    "note": "one position per sequence (S = 1, the AR decoding step) on the same caches: "
+                            "tt_denoise_attn's decode kernel; timed separately, not in the step"},
                 "step_roofline_us": step_roof_us, "step_frac": step_roof_us / (ms / a.steps * 1e3)},
+            "attention_per_committed_token": {
+                "unit": "us of attention per committed token (all sequences of the batch)",
+                "block_diffusion": attn_ms * 1e3 / commits, "ar_decode": dec_ms * 1e3 / cfg.B,
+                "ratio_ar_over_diffusion": (dec_ms / cfg.B) / (attn_ms / commits),
+                "commits_per_step": commits,
+                "note": "diffusion: the S=16 block attention per step / positions the timed steps committed "
+                        "(first denoise step of a fresh block on the synthetic logits); AR: the S=1 attention "
+                        "per step / B (one token per sequence). Per layer; the model's other layers are out "
+                        "of scope"},
             "attention_block_sizes": {
                 f"S{Sv}": s_var_entry(cfg, lens, Sv, us * 1e3, hbm, tc) for Sv, us in s_var.items()},
             "gpu_launches": a.steps * launches_per_step(cfg),
