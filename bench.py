@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--s-variants", action="store_true",
                     help="also time the attention at block sizes S = 32, 64, 128 on the same contexts")
+    ap.add_argument("--loop-blocks", type=int, default=0,
+                    help="(--config loop) blocks per loop instead of the workload's 8 (a smaller run to profile)")
+    ap.add_argument("--loop-steps", type=int, default=0,
+                    help="(--config loop) denoise steps per block instead of the workload's T = 16")
     return ap.parse_args()
 
 
@@ -57,7 +61,7 @@ def parse():
 
 CSRC = os.path.join(ROOT, "block_wise_diffusion_denoise_b300", "csrc")
 PROFILED = {   # kernel -> (summary under profiles/, the sources its counters were taken from)
-    "attention": ("attention_ctx8k.md", ("attn_tc.cu", "sm100_ptx.cuh", "tt_common.cuh")),
+    "attention": ("attention_ctx8k.md", ("attn_tc.cu", "attn_work.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
     "unmask": ("unmask_ctx8k.md", ("unmask.cu", "vocab_stream.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
     "masked_nll": ("masked_nll_ctx8k.md", ("masked_nll.cu", "vocab_stream.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
     "decode": ("decode_attention_ctx8k.md", ("attn_decode.cu", "attn_work.cuh", "sm100_ptx.cuh", "tt_common.cuh")),
@@ -696,6 +700,8 @@ def run_loop(a, cfg):
     dev = torch.device("cuda", local)
     bf = torch.bfloat16
     seed = a.seed + 1000 * rank
+    if a.loop_blocks > 0 or a.loop_steps > 0:
+        cfg = cfg.replace(n_blocks=a.loop_blocks or cfg.n_blocks, T=a.loop_steps or cfg.T)
     B, S, Hq, Hkv, D, V, T, NL, NB = cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.D, cfg.V, cfg.T, cfg.n_layers, cfg.n_blocks
     L0 = cfg.len_lo
     cap = L0 + S * NB
@@ -810,6 +816,44 @@ def run_loop(a, cfg):
         e1.synchronize()
     append_us = e0.elapsed_time(e1) / (10 * NB) * 1e3
 
+    # The attention alone, every layer at the start length: the block (S = 16) and one
+    # autoregressive decoding position (S = 1) per sequence, for the attention cost per
+    # committed token of the two ways of generating.
+    attn_ws = api.workspace(api.tt_denoise_attn_workspace_size(B, S, Hq, Hkv, D, bf), dev)
+    dec_ws = api.workspace(api.tt_denoise_attn_workspace_size(B, 1, Hq, Hkv, D, bf), dev)
+    dec_qkv = [(x[0][:, :1].contiguous(), x[1][:, :1].contiguous(), x[2][:, :1].contiguous()) for x in qkv[0]]
+    dec_out = [torch.empty((B, 1, Hq, D), dtype=bf, device=dev) for _ in range(NL)]
+
+    def layers(stream, decode):
+        for l in range(NL):
+            if decode:
+                q1, k1, v1 = dec_qkv[l]
+                api.tt_denoise_attn(caches[l], q1, k1, v1, out=dec_out[l], sm_scale=sc, ws=dec_ws, dev_err=err,
+                                    stream=stream)
+            else:
+                q, kb, vb = qkv[0][l]
+                api.tt_denoise_attn(caches[l], q, kb, vb, out=outs[l], sm_scale=sc, ws=attn_ws, dev_err=err,
+                                    stream=stream)
+
+    layer_us = {}
+    for decode in (False, True):
+        gl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gl, stream=s_):
+            ctx_len.copy_(ctx0)
+            for _ in range(4):
+                layers(s_, decode)
+        gl.replay()
+        barrier()
+        with torch.cuda.stream(s_):
+            e0.record(s_)
+            for _ in range(5):
+                gl.replay()
+            e1.record(s_)
+            e1.synchronize()
+        layer_us[decode] = e0.elapsed_time(e1) / 20 * 1e3     # all NL layers, one step
+    if api.tt_get_device_error(err) != 0:
+        raise SystemExit("device error in the attention-only timings")
+
     if rank == 0:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
             if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
@@ -850,8 +894,18 @@ def run_loop(a, cfg):
             "steps_with_a_commit": int(steps_done),
             "kernels": {"append": {"us": append_us, "layers": NL,
                                    "bytes": NL * 2 * 2 * B * S * Hkv * D * 2.0,
-                                   "gbs": NL * 2 * 2 * B * S * Hkv * D * 2.0 / (append_us * 1e-6) / 1e9}},
-            "gpu_launches": reps * (nsteps * (NL + 1) + NB),
+                                   "gbs": NL * 2 * 2 * B * S * Hkv * D * 2.0 / (append_us * 1e-6) / 1e9},
+                        "attention_all_layers": {"us": layer_us[False], "context": L0, "S": S},
+                        "decode_attention_all_layers": {"us": layer_us[True], "context": L0, "S": 1}},
+            "attention_per_committed_token": {
+                "unit": "us of attention (all layers) per committed token, whole batch",
+                "block_diffusion": layer_us[False] / (commits.sum().item() / nsteps),
+                "ar_decode": layer_us[True] / B,
+                "ratio_ar_over_diffusion": (layer_us[True] / B) / (layer_us[False] / (commits.sum().item() / nsteps)),
+                "note": "diffusion: the S=16 attention of every layer per denoise step / the loop's mean commits "
+                        "per step; AR: the S=1 attention of every layer per step / B; both at the start context "
+                        "length"},
+            "gpu_launches": reps * (nsteps * (NL + 1) + NB),   # the timed loops (the other timings are extra)
             "graph": True,
             "clocks": sampler.summary(),
         }

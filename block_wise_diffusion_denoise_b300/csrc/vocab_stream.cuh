@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
         // that are not masked; lane 0 issues the copies.
         const T *logits = static_cast<const T *>(c.logits);
         const long long nb = c.nblocks;
+        const uint64_t pol = sm100::policy_evict_first();   // each logit is read once
         int i = 0;                                       // units issued (stage = i % kStages)
         bool ok = true;
         for (long long j = blockIdx.x; ok && j < nb; j += gridDim.x) {
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
                     sh.desc[s] = StageDesc{(int)j, e0, ne / EPV, u == u1 - 1 ? 1 : 0};
                     const uint32_t bytes = (uint32_t)(ne * (int)sizeof(T));
                     sm100::mbar_arrive_expect_tx(&sh.full[s], bytes);
-                    sm100::bulk_load(ring + (size_t)s * kUnitBytes, rowp + e0, bytes, &sh.full[s]);
+                    sm100::bulk_load_hint(ring + (size_t)s * kUnitBytes, rowp + e0, bytes, &sh.full[s], pol);
                 }
                 __syncwarp();
             }
