@@ -654,7 +654,7 @@ def run_ours(a, cfg):
                     "note": "tt_context_block_attn on the same inputs; timed separately, not in the step"},
                 "masked_nll": {
                     "us": nll_ms * 1e3, "gbs": ub / (nll_ms * 1e-3) / 1e9, "hbm_frac": ub / (nll_ms * 1e-3) / 1e9 / hbm,
-                    "roofline_us": ub / (hbm * 1e9) * 1e6,
+                    "roofline_us": ub / (hbm * 1e9) * 1e6, "traffic": profiled_traffic("masked_nll", cfg.name),
                     "note": "tt_masked_nll over the step's logits with every position masked; timed separately, "
                             "not in the step"},
                 "decode_attention": {

@@ -18,12 +18,14 @@
 //    shared-memory stages with plain bulk copies (cp.async.bulk, completion as
 //    transaction bytes on the stage's mbarrier); sixteen consumer warps share every
 //    stage (each thread takes eight 16-byte vectors), so the warps of a CTA move in
-//    step.  A stage is given back when all sixteen warps have read it.
+//    step.  A stage is given back as soon as all sixteen warps have loaded it into
+//    registers, before any arithmetic, so that the next copy into it starts early.  The
+//    bulk copies carry an L2 evict-first policy: every logit is read once.
 //  * Arithmetic.  Per thread, in two passes over the unit's vectors in registers: the
 //    maximum (one value per vector by packed bf16 maxima, exact, then three-input fp32
-//    maxima), the first index holding it (only when it rises: the vector holding it is
-//    re-read from the stage), then sum 2^(x*log2e - mc) over eight scalar
-//    accumulators, one FMA per value, with mc = m*log2e rounded to fp32.  Every term then
+//    maxima), the first index holding it (only when it rises), then sum
+//    2^(x*log2e - mc) over eight scalar accumulators, two values per paired FMA and
+//    paired add, with mc = m*log2e rounded to fp32.  Every term then
 //    carries the same factor 2^delta, delta = m*log2e - mc, which one FMA gives exactly
 //    and one exponential removes at the end of the block (below 2^-3 in magnitude while
 //    |m| < 2^20; for larger logits the terms take the difference first, (x - m)*log2e,

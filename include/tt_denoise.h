@@ -159,11 +159,16 @@ TT_API tt_status tt_denoise_attn_workspace_size(int B, int S, int Hq, int Hkv, i
  *          share the work (1 = no split of any sequence's context)
  * ws, ws_bytes  device workspace of at least tt_denoise_attn_workspace_size bytes
  *
- * Supported: S >= 1, Hq % Hkv == 0, D in {32, 64, 128}.  bf16 with D = 128,
- * page_size = 64, S a multiple of 16 up to 128 and (Hq/Hkv)*S a multiple of 128
- * up to 2048 runs on the tensor-core kernel; every other supported shape (and
- * all of fp32) runs on the CUDA-core kernel.  Other shapes return
- * TT_ERR_UNSUPPORTED. */
+ * S = 1 is one step of autoregressive decoding from the same cache (the token's
+ * own key and value are the "block" keys): the baseline the pages compare the
+ * block-wise diffusion against (dgnews.ru, "What the tests actually show").
+ *
+ * Supported: S >= 1, Hq % Hkv == 0, D in {32, 64, 128}.  With bf16, D = 128,
+ * page_size = 64 and sm_scale > 0, two tensor-core kernels serve: S a multiple
+ * of 16 up to 128 with (Hq/Hkv)*S a multiple of 128 up to 2048 (the block
+ * kernel), and S = 1 with Hq/Hkv = 16 (the decode kernel; its workspace is sized
+ * by the same function for S = 1).  Every other supported shape (and all of
+ * fp32) runs on the CUDA-core kernel.  Other shapes return TT_ERR_UNSUPPORTED. */
 TT_API tt_status tt_denoise_attn(const tt_kv_cache *ctx, const void *q, const void *k_blk,
                           const void *v_blk, void *out, float *lse, int B, int S, int Hq,
                           float sm_scale, int max_ctas, void *ws, size_t ws_bytes,

@@ -83,10 +83,16 @@ def test_reference_arm_line_keeps_the_contract(capsys, monkeypatch):
     assert line["metric"] == b.METRIC and line["unit"] == "steps/s" and line["higher_is_better"] is True
     assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
     assert line["scaling"] == "weak" and line["vs_baseline"] is None and line["dtype"] == "f64"
-    assert line["ms_per_step"] == pytest.approx(1e3 / line["value"])
+    # a step is a timed sample of the batch step: ms_per_step is what the run spent per step
+    # (the steps fit in the run's own wall time), value scales it to the whole batch
+    assert line["full_step_ms"] == pytest.approx(1e3 / line["value"])
+    assert line["sample_fraction"] == pytest.approx(line["ms_per_step"] / line["full_step_ms"])
+    assert 0 < line["sample_fraction"] < 1
+    assert line["steps"] * line["ms_per_step"] <= line["wall_s"] * 1e3 * 1.001
     assert line["config"]["workload"].startswith("single:")
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert cb["cpu"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == "steps/s"
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
