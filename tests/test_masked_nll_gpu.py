@@ -151,6 +151,15 @@ def test_masked_nll_large_batch_and_bad_target():
     assert np.isfinite(nll[4][masked[4]]).all()
 
 
+def test_masked_nll_batch_above_the_flag_snapshot():
+    """17600 rows, more than the 16384 masked flags the pass copies into shared memory."""
+    cfg = synth.CONFIGS["single"].replace(B=1100, V=1024)
+    lg = synth.draw_logits(cfg, seed=9, peak_hi=15.0)
+    clean, u, t = synth.draw_corruption(cfg, seed=9)
+    masked = np.stack([oracle.linear_schedule_mask(u[b], float(t[b])) for b in range(cfg.B)])
+    _check_nll(lg, "bf16", clean, masked)
+
+
 def test_masked_nll_rejects_unaligned_rows():
     lg = torch.zeros((2, 16, 1003), dtype=torch.bfloat16, device="cuda")
     m = torch.ones((2, 16), dtype=torch.uint8, device="cuda")

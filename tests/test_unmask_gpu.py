@@ -144,6 +144,20 @@ def test_nothing_masked_and_empty_batch():
     torch.cuda.synchronize()
 
 
+def test_batch_above_the_flag_snapshot(stats):
+    """1100 sequences x 16 positions = 17600 rows, more than the 16384 masked flags the pass
+    copies into shared memory: its producer and publisher read the flags from global memory."""
+    cfg = synth.CONFIGS["single"].replace(B=1100, V=1024)
+    rng = np.random.default_rng(11)
+    lg = synth.draw_logits(cfg, seed=21, peak_hi=30.0)
+    masked = (rng.random((cfg.B, cfg.S)) < 0.6).astype(np.uint8)
+    masked[:5] = 0                                   # sequences with nothing masked
+    masked[-3:] = 1
+    tokens = np.where(masked == 1, -1, 5).astype(np.int32)
+    for step in (1, cfg.T):
+        _check_step(lg, "bf16", masked, tokens, cfg.tau, step, cfg.T, stats=stats)
+
+
 def test_large_batch(stats):
     """260 sequences (4160 rows, more blocks than the grid has CTAs many times over); mixed
     masked rows, a few sequences with nothing masked, every branch of the rules."""
