@@ -611,7 +611,10 @@ def run_ours(a, cfg):
         e_ms = e0.elapsed_time(e1) / a.e2e_steps
         e_ms = max_over_ranks(e_ms, world, dev)
         e2e = {"value": job_rate(world, 1, e_ms), "unit": "steps/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": a.e2e_steps}
+               "d2h_bytes_per_step": int(d2h), "steps": a.e2e_steps,
+               "link_gbs": (h2d + d2h) / (e_ms * 1e-3) / 1e9,
+               "note": "bound by the host link: the step's logits cross it every step; link_gbs = bytes "
+                       "moved per step / the step's time"}
 
     if rank == 0:
         import json as _json
