@@ -119,3 +119,15 @@ def test_repeated_calls_share_one_workspace():
     for _ in range(3):
         assert torch.equal(_run(cfg, *case, ws=ws)[3].view(torch.int16), first.view(torch.int16))
     assert int(ws[:256].view(torch.int32).abs().sum()) == 0
+
+
+@pytest.mark.parametrize("name,kw", [("tiny", {}), ("single", {"Hq": 16, "Hkv": 2}),
+                                     ("single", {"Hq": 64, "Hkv": 2})])
+def test_one_position_on_the_cuda_core_kernel(name, kw):
+    """S = 1 shapes the decode kernel does not take (fp32; 8 or 32 query heads per KV head)
+    run on the CUDA-core kernel, against the same oracle."""
+    cfg = _cfg(name, B=3, qkv_scale=1.0, **kw)
+    lens = [cfg.len_lo, 1, 0] if name == "tiny" else [700, 129, 0]
+    cache, q, kb, vb = support.attention_case(cfg, seed=31, lens=lens)
+    tol = 1e-5 if cfg.dtype == "f32" else 2e-2
+    _check(cfg, cache, q, kb, vb, tol=tol)
