@@ -48,8 +48,10 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--s-variants", action="store_true",
-                    help="also time the attention at block sizes S = 32, 64, 128 on the same contexts")
+    ap.add_argument("--s-variants", dest="s_variants", action="store_true", default=True,
+                    help="also time the attention at block sizes S = 32, 64, 128 on the same contexts (default)")
+    ap.add_argument("--no-s-variants", dest="s_variants", action="store_false",
+                    help="skip the block-size timings")
     ap.add_argument("--loop-blocks", type=int, default=0,
                     help="(--config loop) blocks per loop instead of the workload's 8 (a smaller run to profile)")
     ap.add_argument("--loop-steps", type=int, default=0,
