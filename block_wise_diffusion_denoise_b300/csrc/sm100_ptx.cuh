@@ -57,18 +57,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
-// Warp-uniform form of mbar_wait: every lane polls (so every lane observes the phase and
-// its data), and the loop ends for all lanes together -- true once every lane has seen the
-// phase complete, false for all after `limit` rounds.  Call with the whole warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint32_t limit) {
-    bool done = false;
-    for (uint32_t i = 0; i < limit; ++i) {
-        if (!done) done = mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, done)) return true;
-    }
-    return false;
-}
-
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -303,14 +291,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// Load with acquire semantics at GPU scope: orders the caller's later reads after the
-// writes released by whoever wrote (or extended the release sequence of) the value read.
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *ptr) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
 }
 
 // Fetch-and-add with acquire-release semantics at GPU scope: releases the calling
