@@ -208,9 +208,14 @@ __device__ __forceinline__ void row_state(const Common &c, long long row, float 
 #pragma unroll
         for (int k = 0; k < 4; ++k) merge_state(m, z, a, v[k].x, v[k].y, __float_as_int(v[k].z));
     }
-    for (; g < c.bpr; ++g) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + g));
-        merge_state(m, z, a, v.x, v.y, __float_as_int(v.z));
+    if (g < c.bpr) {   // the last one to three, also loaded together (merged in block order)
+        float4 v[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+            if (g + k < c.bpr) v[k] = __ldcg(reinterpret_cast<const float4 *>(pp + g + k));
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+            if (g + k < c.bpr) merge_state(m, z, a, v[k].x, v[k].y, __float_as_int(v[k].z));
     }
 }
 
