@@ -37,7 +37,10 @@
 //  * Completion.  A consumer warp hands its state at the end of a block to a publisher
 //    warp through a small ring in shared memory and moves on; the publisher merges the
 //    sixteen states of a block, writes its partial and adds one to the sequence's ticket
-//    (acquire-release; a batch of blocks from its lanes at once).  The add that brings the
+//    (acquire-release; a batch of blocks from its lanes at once).  While the copies
+//    stream, the release and the add take several microseconds, longer than the
+//    consumers take for a block, so two publisher warps take alternate ring entries and
+//    their round trips overlap.  The add that brings the
 //    ticket to (masked rows of the sequence) x (blocks per row) runs the Finish policy for
 //    that sequence, which merges each masked row's partials in block order -- so the
 //    result does not depend on which CTA processed which block -- and resets the ticket.
@@ -63,9 +66,11 @@ namespace vs {
 constexpr int kConsumerWarps = 16;                  // four per SM sub-partition
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kProducerWarp = kConsumerWarps;       // moves the data
-constexpr int kPublisherWarp = kConsumerWarps + 1;  // publishes finished blocks
-constexpr int kThreads = kConsumers + 64;
-constexpr int kRed = 16;                            // finished blocks awaiting the publisher
+constexpr int kPublisherWarp = kConsumerWarps + 1;  // the first of the warps that publish finished blocks
+constexpr int kPublishers = 2;                      // publisher p takes ring entries p, p + 2, ...
+constexpr int kThreads = kConsumers + 32 + 32 * kPublishers;
+constexpr int kRed = 16;                            // finished blocks awaiting the publishers
+static_assert(kRed % kPublishers == 0, "each ring slot belongs to one publisher");
 constexpr int kUnitBytes = 65536;
 constexpr int kVecPerThread = kUnitBytes / 16 / kConsumers;   // 8
 constexpr int kStages = 3;
@@ -381,23 +386,26 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
         for (long long r = tid; r < rows; r += kThreads) snap[r] = c.masked[r];
     __syncthreads();
 
-    if (warp == kPublisherWarp) {
-        // ================================================================ publisher (one warp)
-        // Takes the finished blocks in the order the consumers finish them, up to 16 at a
-        // time, one per lane: the lane merges the block's sixteen warp states (in warp order),
-        // writes the block's partial and adds it to its sequence's ticket with an
-        // acquire-release atomic, so a batch costs one round trip; a lane whose add completes
-        // a sequence has the warp run that sequence's Finish.  No consumer waits on this.
-        int k = 0;                                   // next finished block of this CTA
+    if (warp >= kPublisherWarp) {
+        // ================================================================ publishers
+        // Publisher p takes the ring entries p, p + kPublishers, ... (every slot of the ring
+        // belongs to one publisher): the finished blocks in the order the consumers finish
+        // them, up to kRed / kPublishers at a time, one per lane.  The lane merges the
+        // block's sixteen warp states (in warp order), writes the block's partial and adds
+        // it to its sequence's ticket with an acquire-release atomic, so a batch costs one
+        // round trip; a lane whose add completes a sequence has the warp run that sequence's
+        // Finish.  No consumer waits on this.
+        const int pw = warp - kPublisherWarp;
+        int k = pw;                                  // next finished block of this CTA for this warp
         bool more = true;
         while (more) {
             if (!wait_or_abort(sh, &sh.red_full[k % kRed], (uint32_t)(k / kRed) & 1, c.dev_err)) break;
-            // the ready prefix of entries k, k+1, ... (entry k is ready)
-            const int e = k + lane;
-            const bool ready = lane < kRed && (lane == 0 || sm100::mbar_try_wait(&sh.red_full[e % kRed],
-                                                                                 (uint32_t)(e / kRed) & 1));
+            // the ready prefix of entries k, k+P, k+2P, ... (entry k is ready)
+            const int e = k + kPublishers * lane;
+            const bool ready = lane < kRed / kPublishers &&
+                               (lane == 0 || sm100::mbar_try_wait(&sh.red_full[e % kRed], (uint32_t)(e / kRed) & 1));
             const unsigned rb = __ballot_sync(0xffffffffu, ready);
-            const int n = __ffs(~rb) - 1;            // entries k .. k+n-1 are ready (n >= 1)
+            const int n = __ffs(~rb) - 1;            // n >= 1 of this warp's entries are ready
             int b = -1;
             unsigned last = 0;
             const bool mine = lane < n;
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
                 __syncwarp();
                 if (lane == 0) c.tickets[bs] = 0;   // ready for the next launch
             }
-            k += n;
+            k += kPublishers * n;
         }
         return;
     }
@@ -499,11 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
         if (!wait_or_abort(sh, &sh.full[s], (uint32_t)(i / kStages) & 1, c.dev_err)) break;
         const StageDesc d = sh.desc[s];
         if (d.blk < 0) {
-            // no more work: hand the publisher the end marker
-            const int r = kb % kRed;
-            if (wait_or_abort(sh, &sh.red_empty[r], ((uint32_t)(kb / kRed) & 1) ^ 1, c.dev_err) && lane == 0) {
-                if (warp == 0) sh.red_blk[r] = -1;
-                sm100::mbar_arrive(&sh.red_full[r]);
+            // no more work: hand every publisher an end marker (the next entry of each)
+            for (int e = kb; e < kb + kPublishers; ++e) {
+                const int r = e % kRed;
+                if (!wait_or_abort(sh, &sh.red_empty[r], ((uint32_t)(e / kRed) & 1) ^ 1, c.dev_err)) break;
+                if (lane == 0) {
+                    if (warp == 0) sh.red_blk[r] = -1;
+                    sm100::mbar_arrive(&sh.red_full[r]);
+                }
             }
             break;
         }
