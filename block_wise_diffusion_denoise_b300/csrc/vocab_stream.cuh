@@ -390,9 +390,11 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
         // ================================================================ publishers
         // Publisher p takes the ring entries p, p + kPublishers, ... (every slot of the ring
         // belongs to one publisher): the finished blocks in the order the consumers finish
-        // them, up to kRed / kPublishers at a time, one per lane.  The lane merges the
-        // block's sixteen warp states (in warp order), writes the block's partial and adds
-        // it to its sequence's ticket with an acquire-release atomic, so a batch costs one
+        // them, up to kRed / kPublishers at a time.  The sixteen warp states of a block are
+        // merged by a half-warp, one state per lane, in a fixed butterfly (merge_state gives
+        // both partners the same bits, so every lane of the half ends with the block's
+        // state); lane j then holds entry j's result, writes the block's partial and adds it
+        // to its sequence's ticket with an acquire-release atomic, so a batch costs one
         // round trip; a lane whose add completes a sequence has the warp run that sequence's
         // Finish.  No consumer waits on this.
         const int pw = warp - kPublisherWarp;
@@ -403,27 +405,45 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
             // the ready prefix of entries k, k+P, k+2P, ... (entry k is ready)
             const int e = k + kPublishers * lane;
             const bool ready = lane < kRed / kPublishers &&
-                               (lane == 0 || sm100::mbar_try_wait(&sh.red_full[e % kRed], (uint32_t)(e / kRed) & 1));
+                               (lane == 0 || sm100::mbar_test_wait(&sh.red_full[e % kRed], (uint32_t)(e / kRed) & 1));
             const unsigned rb = __ballot_sync(0xffffffffu, ready);
             const int n = __ffs(~rb) - 1;            // n >= 1 of this warp's entries are ready
+            // entries j0 and j0 + 1 by the two half-warps at a time; lane j keeps entry j's state
+            float pm = -INFINITY, pz = 0.f;
+            int pa = INT_MAX, pblk = -1;
+            bool ended = false;
+            for (int j0 = 0; j0 < n; j0 += 2) {
+                const int j = j0 + (lane >> 4);
+                const int r = (k + kPublishers * j) % kRed;
+                const int blk = j < n ? sh.red_blk[r] : -1;
+                float M = -INFINITY, Z = 0.f;
+                int A = INT_MAX;
+                if (blk >= 0) { M = sh.red_m[r][lane & 15]; Z = sh.red_z[r][lane & 15]; A = sh.red_a[r][lane & 15]; }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, M, o), z2 = __shfl_xor_sync(0xffffffffu, Z, o);
+                    const int a2 = __shfl_xor_sync(0xffffffffu, A, o);
+                    merge_state(M, Z, A, m2, z2, a2);
+                }
+                // every lane of the half has read the entry (the shuffles above): reusable
+                if ((lane & 15) == 0 && blk >= 0) sm100::mbar_arrive(&sh.red_empty[r]);
+                ended = ended || (j < n && blk < 0);
+                const int from = lane == j0 + 1 ? 16 : 0;
+                const float sm_ = __shfl_sync(0xffffffffu, M, from), sz = __shfl_sync(0xffffffffu, Z, from);
+                const int sa = __shfl_sync(0xffffffffu, A, from), sb = __shfl_sync(0xffffffffu, blk, from);
+                if (lane == j0 || (lane == j0 + 1 && j0 + 1 < n)) { pm = sm_; pz = sz; pa = sa; pblk = sb; }
+            }
             int b = -1;
             unsigned last = 0;
-            const bool mine = lane < n;
-            int blk = mine ? sh.red_blk[e % kRed] : -1;
-            if (mine && blk >= 0) {
-                const int r = e % kRed;
-                float M = sh.red_m[r][0], Z = sh.red_z[r][0];
-                int A = sh.red_a[r][0];
-                for (int w = 1; w < kConsumerWarps; ++w) merge_state(M, Z, A, sh.red_m[r][w], sh.red_z[r][w], sh.red_a[r][w]);
-                sm100::mbar_arrive(&sh.red_empty[r]);        // the entry is read: reusable
+            if (lane < n && pblk >= 0) {
                 UnmaskPartial q;
-                q.m = M; q.z = Z; q.arg = A; q.pad = 0;
-                c.part[blk] = q;
-                b = blk / c.bpr / c.S;
+                q.m = pm; q.z = pz; q.arg = pa; q.pad = 0;
+                c.part[pblk] = q;
+                b = pblk / c.bpr / c.S;
                 const unsigned target = (unsigned)masked_rows(c, snap, use_snap, b) * (unsigned)c.bpr;
                 last = (sm100::atom_add_acq_rel_gpu(&c.tickets[b], 1u) + 1u == target) ? 1u : 0u;
             }
-            more = !__any_sync(0xffffffffu, mine && blk < 0);   // the end marker stops the loop
+            more = !__any_sync(0xffffffffu, ended);   // the end marker stops the loop
             // Finish every sequence this batch completed, one at a time with the whole warp
             // (the completing lane's acquire-release add acquired every block's partial; the
             // warp barrier orders the other lanes' reads after it)
