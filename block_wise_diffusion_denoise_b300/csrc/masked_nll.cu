@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(256) linear_schedule_kernel(const int32_t *cle
 
 size_t masked_nll_ws_bytes(int B, int S, int V, tt_dtype dtype) {
     const size_t part = align_up((size_t)vs::blocks_of(B, S, V, dtype) * sizeof(UnmaskPartial), 256);
-    return part + align_up((size_t)B * sizeof(unsigned), 256);
+    return part + align_up((size_t)(B + 1) * sizeof(unsigned), 256);   // tickets, block counter
 }
 
 tt_status launch_masked_nll(const void *logits, tt_dtype dtype, int B, int S, int V, const int32_t *targets,

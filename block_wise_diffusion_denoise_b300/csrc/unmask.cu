@@ -398,7 +398,7 @@ int unmask_chunk_elems(tt_dtype dtype) { return kChunkBytes / (dtype == TT_BF16 
 
 // Workspace: partial slots at offset 0 (one per (row, 32 KB chunk) for the chunked kernel,
 // one per block for the streaming pass; the larger count is reserved), then the
-// per-sequence tickets.
+// per-sequence tickets and the streaming pass's block counter.
 size_t unmask_tickets_off(int B, int S, int V, tt_dtype dtype) {
     const size_t nchunk = (size_t)((V + unmask_chunk_elems(dtype) - 1) / unmask_chunk_elems(dtype));
     const size_t chunked = (size_t)B * S * nchunk;
@@ -407,7 +407,7 @@ size_t unmask_tickets_off(int B, int S, int V, tt_dtype dtype) {
 }
 
 size_t unmask_ws_bytes(int B, int S, int V, tt_dtype dtype) {
-    return unmask_tickets_off(B, S, V, dtype) + align_up((size_t)B * sizeof(unsigned), 256);
+    return unmask_tickets_off(B, S, V, dtype) + align_up((size_t)(B + 1) * sizeof(unsigned), 256);
 }
 
 tt_status launch_unmask(const void *logits, tt_dtype dtype, int B, int S, int V, float tau,

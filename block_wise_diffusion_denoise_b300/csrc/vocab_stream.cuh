@@ -9,11 +9,13 @@
 // Design (HBM-bound; every masked logit is read once):
 //  * Work.  A row of V logits is cut into units of 64 KB; up to kUnitsPerBlock
 //    consecutive units of one row form a block, the grain of the partial results.
-//    Blocks are numbered over every (row, unit group) of the batch in row order, and CTA
-//    c takes blocks c, c + grid, c + 2 grid, ... (balanced to within one block), skipping
-//    those of rows that are not masked (a copy of the flags in shared memory).  The grid
-//    walks the blocks in row order together, so sequences complete one after another
-//    during the launch and their finishing work overlaps the streaming of later ones.
+//    The blocks of masked rows are ranked in row order (from a copy of the flags in
+//    shared memory); CTA c takes rank c, then one rank after another from a counter in
+//    the workspace, so the CTAs that the memory system serves faster take more blocks
+//    and all of them run dry together (a static share left the last CTAs about 4 us
+//    behind the first).  The grid walks the blocks in row order together, so sequences
+//    complete one after another during the launch and their finishing work overlaps the
+//    streaming of later ones.
 //  * Pipeline.  One producer warp moves units into a CTA-wide ring of kStages
 //    shared-memory stages with plain bulk copies (cp.async.bulk, completion as
 //    transaction bytes on the stage's mbarrier); sixteen consumer warps share every
@@ -185,6 +187,7 @@ struct Shared {
     float red_m[kRed][kConsumerWarps], red_z[kRed][kConsumerWarps];
     int red_a[kRed][kConsumerWarps];
     int red_blk[kRed];                           // block id, or -1: no more blocks
+    int warp_masked[kThreads / 32];              // masked rows each warp found in the snapshot
     int abort;
 };
 
@@ -382,8 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
     uint8_t *snap = ring + (size_t)kStages * kUnitBytes;
     const long long rows = (long long)c.B * c.S;
     const bool use_snap = rows <= kMaskSnap;
+    int my_masked = 0;
     if (use_snap)
-        for (long long r = tid; r < rows; r += kThreads) snap[r] = c.masked[r];
+        for (long long r = tid; r < rows; r += kThreads) {
+            const uint8_t v = c.masked[r];
+            snap[r] = v;
+            my_masked += v != 0 ? 1 : 0;
+        }
+    my_masked = (int)__reduce_add_sync(0xffffffffu, (unsigned)my_masked);
+    if (lane == 0) sh.warp_masked[warp] = my_masked;
     __syncthreads();
 
     if (warp >= kPublisherWarp) {
@@ -391,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
         // Publisher p takes the ring entries p, p + kPublishers, ... (every slot of the ring
         // belongs to one publisher): the finished blocks in the order the consumers finish
         // them, up to kRed / kPublishers at a time.  The sixteen warp states of a block are
-        // merged by a half-warp, one state per lane, in a fixed butterfly (merge_state gives
-        // both partners the same bits, so every lane of the half ends with the block's
-        // state); lane j then holds entry j's result, writes the block's partial and adds it
+        // merged by a half-warp, one state per lane, the way a consumer warp reduces its
+        // lanes (every lane of the half ends with the same bits); lane j then holds entry
+        // j's result, writes the block's partial and adds it
         // to its sequence's ticket with an acquire-release atomic, so a batch costs one
         // round trip; a lane whose add completes a sequence has the warp run that sequence's
         // Finish.  No consumer waits on this.
@@ -419,12 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
                 float M = -INFINITY, Z = 0.f;
                 int A = INT_MAX;
                 if (blk >= 0) { M = sh.red_m[r][lane & 15]; Z = sh.red_z[r][lane & 15]; A = sh.red_a[r][lane & 15]; }
+                // as a consumer warp reduces its lanes: the half's maximum, one rescale per
+                // lane, a butterfly sum (the same bits in every lane) and the lowest index
+                int key = f2key(M);
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xffffffffu, M, o), z2 = __shfl_xor_sync(0xffffffffu, Z, o);
-                    const int a2 = __shfl_xor_sync(0xffffffffu, A, o);
-                    merge_state(M, Z, A, m2, z2, a2);
-                }
+                for (int o = 8; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+                const float Mb = key2f(key);
+                float zt = (M == -INFINITY) ? 0.f : Z * fast_exp2((M - Mb) * kLog2e);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) zt += __shfl_xor_sync(0xffffffffu, zt, o);
+                int at = (Mb != -INFINITY && M == Mb) ? A : INT_MAX;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) at = min(at, __shfl_xor_sync(0xffffffffu, at, o));
+                M = Mb;
+                Z = zt;
+                A = at;
                 // every lane of the half has read the entry (the shuffles above): reusable
                 if ((lane & 15) == 0 && blk >= 0) sm100::mbar_arrive(&sh.red_empty[r]);
                 ended = ended || (j < n && blk < 0);
@@ -464,18 +483,27 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
 
     if (warp == kProducerWarp) {
         // ================================================================ producer (one warp)
-        // CTA c takes blocks c, c + grid, c + 2 grid, ... (the grid covers every block in
-        // row order at once, so sequences complete one after another) and skips those of rows
-        // that are not masked; lane 0 issues the copies.
+        // With the flags in shared memory, the blocks of masked rows are handed out in row
+        // order by rank: CTA c takes rank c first, then each next rank from a counter in the
+        // workspace (one atomic per block, issued when the block before starts, so its round
+        // trip hides behind the copies); CTAs that get more bandwidth take more blocks and
+        // all of them run out of work together.  A rank is turned into its row by a forward
+        // scan of the flags (ranks only grow within a CTA).  Every block takes exactly one
+        // atomic, so the one that returns the last value resets the counter for the next
+        // launch.  Without the copy of the flags (very large batches), CTA c takes blocks c,
+        // c + grid, c + 2 grid, ... and skips those of rows that are not masked.  Lane 0
+        // issues the copies.
         const T *logits = static_cast<const T *>(c.logits);
-        const long long nb = c.nblocks;
         const uint64_t pol = sm100::policy_evict_first();   // each logit is read once
         int i = 0;                                       // units issued (stage = i % kStages)
         bool ok = true;
-        for (long long j = blockIdx.x; ok && j < nb; j += gridDim.x) {
+        // the copies of block j (row j / bpr, its units u0 .. u1 - 1); after the first one,
+        // lane 0 takes the CTA's next rank from the counter (when one is given)
+        unsigned *counter = c.tickets + c.B;
+        unsigned nxt = 0;
+        auto issue = [&](long long j, bool grab) {
             const long long row = j / c.bpr;
             const int g = (int)(j % c.bpr);
-            if ((use_snap ? snap[row] : c.masked[row]) == 0) continue;   // nothing to read
             const int u0 = g * kUnitsPerBlock, u1 = min(c.nc, u0 + kUnitsPerBlock);
             const T *rowp = logits + row * (long long)c.V;
             for (int u = u0; u < u1; ++u, ++i) {
@@ -490,8 +518,48 @@ __global__ void __launch_bounds__(kThreads, 1) vocab_stream_kernel(const Common 
                     const uint32_t bytes = (uint32_t)(ne * (int)sizeof(T));
                     sm100::mbar_arrive_expect_tx(&sh.full[s], bytes);
                     sm100::bulk_load_hint(ring + (size_t)s * kUnitBytes, rowp + e0, bytes, &sh.full[s], pol);
+                    if (grab && u == u0) nxt = atomicAdd(counter, 1u);   // in flight during the block
                 }
                 __syncwarp();
+            }
+        };
+        if (use_snap) {
+            const int nmr = (int)__reduce_add_sync(0xffffffffu, lane < kThreads / 32 ? (unsigned)sh.warp_masked[lane] : 0u);
+            const long long total = (long long)nmr * c.bpr;   // blocks of masked rows
+            const int nrows = (int)rows;
+            int cur_row = 0, cur_cnt = 0;                     // rows [0, cur_row) hold cur_cnt masked rows
+            long long r = blockIdx.x;                         // rank among the blocks of masked rows
+            while (ok && r < total) {
+                const long long q = r / c.bpr;                 // the q-th masked row
+                int row = -1;
+                while (cur_row < nrows) {
+                    const int rr = cur_row + lane;
+                    const bool mk = rr < nrows && snap[rr] != 0;
+                    const unsigned bal = __ballot_sync(0xffffffffu, mk);
+                    const int cnt = __popc(bal);
+                    if (q < cur_cnt + cnt) {
+                        const bool hit = mk && __popc(bal & ((1u << lane) - 1u)) == (int)(q - cur_cnt);
+                        row = cur_row + __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+                        break;
+                    }
+                    cur_cnt += cnt;
+                    cur_row += 32;
+                }
+                if (row < 0) {   // cannot happen: the ranks are below the count of the same flags
+                    if (lane == 0) report_error(c.dev_err, TT_ERR_BOUNDS);
+                    ok = false;
+                    break;
+                }
+                issue((long long)row * c.bpr + r % c.bpr, true);
+                if (!ok) break;   // the grab may not have happened: the counter is left to the error
+                const unsigned v = __shfl_sync(0xffffffffu, nxt, 0);
+                if (lane == 0 && (long long)v == total - 1) *counter = 0u;   // the launch's last atomic
+                r = (long long)gridDim.x + v;
+            }
+        } else {
+            for (long long j = blockIdx.x; ok && j < c.nblocks; j += gridDim.x) {
+                if (c.masked[j / c.bpr] == 0) continue;   // nothing to read
+                issue(j, false);
             }
         }
         // end of the work: a stage without data
@@ -585,8 +653,9 @@ inline bool rows_aligned(const void *logits, int V, tt_dtype dtype) {
 }
 
 // One launch of the pass with the Finish policy Fin; the workspace pieces are the caller's
-// (part: blocks_of() slots, tickets: B words, zero before the first launch and left zero
-// by every launch that completes).
+// (part: blocks_of() slots; tickets: B + 1 words, the sequences' tickets and then the
+// block counter, zero before the first launch and left zero by every launch that
+// completes).
 template <class Fin>
 tt_status launch(const typename Fin::Params &f, const void *logits, tt_dtype dtype, int B, int S, int V,
                  const uint8_t *masked, UnmaskPartial *part, unsigned *tickets, uint32_t *dev_err,
