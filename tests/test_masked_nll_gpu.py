@@ -167,3 +167,31 @@ def test_masked_nll_rejects_unaligned_rows():
     with pytest.raises(api.TTError) as e:
         api.tt_masked_nll(lg, tg, m)
     assert e.value.status == N.TT_ERR_UNSUPPORTED
+
+
+def test_counters_are_left_zero_between_calls():
+    """The tickets and the block counter of the streaming pass (the workspace's last (B + 1)
+    words, padded to 256 bytes) are zero after every call; a second call on the same
+    workspace with another mask still reads every masked row."""
+    B, S, V = 40, 16, 40000
+    cfg = synth.CONFIGS["ctx8k"].replace(B=B, V=V)
+    lg = synth.draw_logits(cfg, seed=8, peak_hi=25.0)
+    rng = np.random.default_rng(8)
+    targets = rng.integers(0, V, (B, S)).astype(np.int32)
+    dev = support.to_dev(lg, "bf16")
+    err = api.error_word()
+    ws = api.workspace(api.tt_masked_nll_workspace_size(B, S, V, torch.bfloat16))
+    tail = ((B + 1) * 4 + 255) // 256 * 256
+    for call in range(2):
+        masked = (rng.random((B, S)) < (0.3 if call == 0 else 0.9)).astype(np.uint8)
+        nll, tot, cnt = api.tt_masked_nll(dev, torch.from_numpy(targets).cuda(), torch.from_numpy(masked).cuda(),
+                                          ws=ws, dev_err=err)
+        assert api.tt_get_device_error(err) == 0
+        w_nll, w_tot, w_cnt = oracle.masked_nll(lg, targets, masked, "bf16")
+        got = nll.cpu().numpy()
+        sel = masked == 1
+        assert np.array_equal(cnt.cpu().numpy(), w_cnt)
+        assert np.all(np.abs(got[sel] - w_nll[sel]) <= NLL_TOL * np.maximum(1.0, np.abs(w_nll[sel])))
+        assert np.isnan(got[~sel]).all()
+        torch.cuda.synchronize()
+        assert int(ws[-tail:].abs().sum()) == 0, call

@@ -169,3 +169,25 @@ def test_large_batch(stats):
     tokens = np.where(masked == 1, -1, 77).astype(np.int32)
     for step in (1, 5, cfg.T):
         _check_step(lg, "bf16", masked, tokens, cfg.tau, step, cfg.T, stats=stats)
+
+
+@pytest.mark.parametrize("B", [31, 64])
+def test_counters_are_left_zero_and_the_next_call_sees_every_block(B, stats):
+    """The streaming pass hands the blocks of masked rows out from a counter in the workspace;
+    the sequences' tickets and that counter must end every launch at zero (they are the
+    workspace's last (B + 1) words, padded to 256 bytes), or the next call would skip blocks.
+    Three calls on one workspace with different masks (a sequence with no masked row, rows
+    masked at random, then every row), each checked against the oracle."""
+    cfg = synth.CONFIGS["ctx8k"].replace(B=B, V=40000)   # two units per row, the second ragged
+    ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.bfloat16))
+    tail = ((B + 1) * 4 + 255) // 256 * 256
+    rng = np.random.default_rng(B)
+    for call in range(3):
+        lg = synth.draw_logits(cfg, seed=40 + call, peak_hi=30.0)
+        masked = (rng.random((cfg.B, cfg.S)) < 0.6).astype(np.uint8) if call < 2 else np.ones((cfg.B, cfg.S), np.uint8)
+        if call == 0:
+            masked[3] = 0
+        tokens = np.where(masked == 1, -1, 5).astype(np.int32)
+        _check_step(lg, "bf16", masked, tokens, cfg.tau, 2, cfg.T, ws, stats)
+        torch.cuda.synchronize()
+        assert int(ws[-tail:].abs().sum()) == 0, call
