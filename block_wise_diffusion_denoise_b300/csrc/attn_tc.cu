@@ -41,7 +41,7 @@
 //    is written as packed bf16 into its own double-buffered TMEM tile.  The
 //    exponent phase of one tile overlaps the next QK product and the score
 //    phase of the partner's tile.  A register split (setmaxnreg) gives the
-//    softmax warpgroups 216 registers per thread and the role warps 64.
+//    softmax warpgroups 208 registers per thread and the role warps 80.
 //    Columns past the valid keys of a partial tile are masked, and the matching
 //    V rows are zeroed before the PV product, so slots past L never matter.
 //  * Work split.  The batch is a list of segments (b, g), each a run of
@@ -171,10 +171,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Register split between warpgroups: the launch gives 384 x 168 registers; the role
-// warpgroup (warps 0-3) drops to 64 each and the two softmax warpgroups rise to 216
-// each (128 x 64 + 256 x 216 = 63488 <= 64512).
-__device__ __forceinline__ void regs_release() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;"); }
-__device__ __forceinline__ void regs_acquire() { asm volatile("setmaxnreg.inc.sync.aligned.u32 216;"); }
+// warpgroup (warps 0-3) drops to 80 each and the two softmax warpgroups rise to 208
+// each (128 x 80 + 256 x 208 = 63488 <= 64512).  Measured against 64 / 216: the
+// attention 1.4 % and its causal-block view 2 % faster.
+__device__ __forceinline__ void regs_release() { asm volatile("setmaxnreg.dec.sync.aligned.u32 80;"); }
+__device__ __forceinline__ void regs_acquire() { asm volatile("setmaxnreg.inc.sync.aligned.u32 208;"); }
 
 // Scores at columns at or past `valid` become -inf (only the last context tile of a
 // segment and the block tile are partial), so one code path serves every tile.
