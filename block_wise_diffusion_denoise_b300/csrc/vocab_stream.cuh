@@ -13,9 +13,10 @@
 //    shared memory); CTA c takes rank c, then one rank after another from a counter in
 //    the workspace, so the CTAs that the memory system serves faster take more blocks
 //    and all of them run dry together (a static share left the last CTAs about 4 us
-//    behind the first).  The grid walks the blocks in row order together, so sequences
-//    complete one after another during the launch and their finishing work overlaps the
-//    streaming of later ones.
+//    behind the first).  Batches too large for the copy of the flags keep a static
+//    share: CTA c takes blocks c, c + grid, ...  The grid walks the blocks in row order
+//    together, so sequences complete one after another during the launch and their
+//    finishing work overlaps the streaming of later ones.
 //  * Pipeline.  One producer warp moves units into a CTA-wide ring of kStages
 //    shared-memory stages with plain bulk copies (cp.async.bulk, completion as
 //    transaction bytes on the stage's mbarrier); sixteen consumer warps share every
@@ -40,9 +41,9 @@
 //    warp through a small ring in shared memory and moves on; the publisher merges the
 //    sixteen states of a block, writes its partial and adds one to the sequence's ticket
 //    (acquire-release; a batch of blocks from its lanes at once).  While the copies
-//    stream, the release and the add take several microseconds, longer than the
-//    consumers take for a block, so two publisher warps take alternate ring entries and
-//    their round trips overlap.  The add that brings the
+//    stream, a publisher's batch (merge, release, add) takes several microseconds,
+//    longer than the consumers take for a block, so two publisher warps take alternate
+//    ring entries and their round trips overlap.  The add that brings the
 //    ticket to (masked rows of the sequence) x (blocks per row) runs the Finish policy for
 //    that sequence, which merges each masked row's partials in block order -- so the
 //    result does not depend on which CTA processed which block -- and resets the ticket.
