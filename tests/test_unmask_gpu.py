@@ -191,3 +191,36 @@ def test_counters_are_left_zero_and_the_next_call_sees_every_block(B, stats):
         _check_step(lg, "bf16", masked, tokens, cfg.tau, 2, cfg.T, ws, stats)
         torch.cuda.synchronize()
         assert int(ws[-tail:].abs().sum()) == 0, call
+
+
+def test_no_masked_row_then_every_row_on_one_workspace(stats):
+    """A call in which no row is masked hands out no block (the counter is never touched), and
+    the next call on the same workspace, with every row masked, still reads every block."""
+    cfg = synth.CONFIGS["ctx8k"].replace(B=8, V=70000)      # three units per row, two blocks
+    ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.bfloat16))
+    tail = ((cfg.B + 1) * 4 + 255) // 256 * 256
+    lg = synth.draw_logits(cfg, seed=77, peak_hi=30.0)
+    none = np.zeros((cfg.B, cfg.S), np.uint8)
+    tokens = np.full((cfg.B, cfg.S), 9, np.int32)
+    m, t, com, conf, nm = _run_step(lg, "bf16", none, tokens, cfg.tau, 3, cfg.T, ws)
+    assert not m.any() and (t == 9).all() and not com.any() and np.isnan(conf).all() and (nm == 0).all()
+    assert int(ws[-tail:].abs().sum()) == 0
+    full = np.ones((cfg.B, cfg.S), np.uint8)
+    _check_step(lg, "bf16", full, np.full((cfg.B, cfg.S), -1, np.int32), cfg.tau, 3, cfg.T, ws, stats)
+    assert int(ws[-tail:].abs().sum()) == 0
+
+
+def test_largest_batch_with_the_flag_copy(stats):
+    """16384 rows (1024 x 16), the most the pass copies into shared memory: every CTA walks
+    the flags far from its first rank and takes dozens of ranks from the counter.  Rows
+    masked at random, small vocabulary; every sequence checked against the oracle."""
+    cfg = synth.CONFIGS["ctx8k"].replace(B=1024, V=96)
+    rng = np.random.default_rng(5)
+    ws = api.workspace(api.tt_unmask_workspace_size(cfg.B, cfg.S, cfg.V, torch.bfloat16))
+    lg = synth.draw_logits(cfg, seed=55, peak_hi=12.0)
+    masked = (rng.random((cfg.B, cfg.S)) < 0.5).astype(np.uint8)
+    masked[::7] = 0                                       # some sequences with nothing masked
+    tokens = np.where(masked == 1, -1, 3).astype(np.int32)
+    _check_step(lg, "bf16", masked, tokens, cfg.tau, 5, cfg.T, ws, stats)
+    tail = ((cfg.B + 1) * 4 + 255) // 256 * 256
+    assert int(ws[-tail:].abs().sum()) == 0
