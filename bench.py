@@ -56,6 +56,8 @@ def parse():
                     help="(--config loop) blocks per loop instead of the workload's 8 (a smaller run to profile)")
     ap.add_argument("--loop-steps", type=int, default=0,
                     help="(--config loop) denoise steps per block instead of the workload's T = 16")
+    ap.add_argument("--tau", type=float, default=None,
+                    help="confidence threshold instead of the workload's 0.9 (e.g. 0.8, the other operating point)")
     return ap.parse_args()
 
 
@@ -948,6 +950,8 @@ def launches_per_step(cfg) -> int:
 def main():
     a = parse()
     cfg = synth.CONFIGS[WORKLOADS[a.config]]
+    if a.tau is not None:
+        cfg = cfg.replace(tau=a.tau)
     if a.impl == "reference":
         return run_reference(a, cfg)
     if a.config == "loop":
