@@ -324,14 +324,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const uint32_t kbase = smem_u32(sm + kOffKd + st * kTile);
             const uint32_t qb = smem_u32(sm + kOffQd + qbuf * kSmall);
             const uint32_t dcol = tmem + kColSd + 16 * (tt & 1);
+            if (elect_one()) {   // one lane issues the tile's MMAs and their commits
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {   // 16 head dimensions per step
-                const uint64_t da = sdesc_sw128(kbase + (kk >> 2) * (uint32_t)kTileHalf + (kk & 3) * 32, 16, 1024);
-                const uint64_t db = sdesc_sw128(qb + (kk >> 2) * (uint32_t)kSmallHalf + (kk & 3) * 32, 16, 1024);
-                if (elect_one()) mma_bf16_ss(dcol, da, db, idesc_qk, kk > 0);
-                __syncwarp();
-            }
-            if (elect_one()) {
+                for (int kk = 0; kk < 8; ++kk) {   // 16 head dimensions per step
+                    const uint64_t da = sdesc_sw128(kbase + (kk >> 2) * (uint32_t)kTileHalf + (kk & 3) * 32, 16, 1024);
+                    const uint64_t db = sdesc_sw128(qb + (kk >> 2) * (uint32_t)kSmallHalf + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ss(dcol, da, db, idesc_qk, kk > 0);
+                }
                 mma_commit(&bar.s_full[tt & 1]);
                 mma_commit(&bar.k_empty[st]);
                 if (last) mma_commit(&bar.q_empty[qbuf]);
@@ -360,13 +359,12 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             tc_fence_after();
             const uint32_t vbase = smem_u32(vp);
             const uint32_t pb = smem_u32(sm + kOffPd + (tt & 1) * kSmall);
-            for (int kk = 0; kk < nk / 16; ++kk) {   // 16 keys per step
-                const uint64_t da = sdesc_sw128(vbase + kk * 2048, kTileHalf, 1024);
-                const uint64_t db = sdesc_sw128(pb + (kk >> 2) * (uint32_t)kSmallHalf + (kk & 3) * 32, 16, 1024);
-                if (elect_one()) mma_bf16_ss(tmem + kColOd, da, db, idesc_pv, !(j == 0 && kk == 0));
-                __syncwarp();
-            }
-            if (elect_one()) {
+            if (elect_one()) {   // one lane issues the tile's MMAs and their commits
+                for (int kk = 0; kk < nk / 16; ++kk) {   // 16 keys per step
+                    const uint64_t da = sdesc_sw128(vbase + kk * 2048, kTileHalf, 1024);
+                    const uint64_t db = sdesc_sw128(pb + (kk >> 2) * (uint32_t)kSmallHalf + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ss(tmem + kColOd, da, db, idesc_pv, !(j == 0 && kk == 0));
+                }
                 mma_commit(&bar.p_free[tt & 1]);
                 mma_commit(&bar.v_empty[st]);
                 if (last) mma_commit(&bar.o_full);

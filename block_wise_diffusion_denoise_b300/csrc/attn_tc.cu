@@ -31,8 +31,9 @@
 //    tensor memory by the softmax warps once per piece.
 //  * MMAs.  One warp issues S = Q K^T (M 128, N 128 keys, A from tensor
 //    memory), another issues O += P V (M 128, N 128 = D, K 128 keys, A from
-//    tensor memory); one elected lane of a converged warp issues, so the
-//    descriptors stay warp-uniform.
+//    tensor memory); one elected lane of a converged warp issues a tile's eight
+//    MMAs and their commits in one go (electing a lane per MMA, with a warp
+//    barrier after each, measured 2-3 % slower).
 //  * Softmax.  Two warps share each TMEM lane quarter and take alternate tiles,
 //    one thread per row: the row's 128 scores come into registers at once and
 //    S goes back to the QK issuer immediately; the running maximum (log2
@@ -402,13 +403,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 const uint32_t idesc = idesc_bf16_f32(128, nk, false, false);
                 const uint32_t kb = smem_u32(sm + kOffK + kst * kStage);
                 const uint32_t dcol = tmem + kColS;
+                if (elect_one()) {   // one lane issues the tile's MMAs and their commits
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {   // 16 head dimensions per step; Q from TMEM
-                    const uint64_t db = sdesc_sw128(kb + (kk >> 2) * (uint32_t)kHalf + (kk & 3) * 32, 16, 1024);
-                    if (elect_one()) mma_bf16_ts(dcol, tmem + kColQ + 8 * kk, db, idesc, kk > 0);
-                    __syncwarp();
-                }
-                if (elect_one()) {
+                    for (int kk = 0; kk < 8; ++kk) {   // 16 head dimensions per step; Q from TMEM
+                        const uint64_t db = sdesc_sw128(kb + (kk >> 2) * (uint32_t)kHalf + (kk & 3) * 32, 16, 1024);
+                        mma_bf16_ts(dcol, tmem + kColQ + 8 * kk, db, idesc, kk > 0);
+                    }
                     mma_commit(&bar.s_full[t & 1]);
                     mma_commit(&bar.k_empty[kst]);
                     if (j == ntiles - 1) mma_commit(&bar.q_empty);
@@ -449,21 +449,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                 tc_fence_after();
                 const uint32_t v0 = smem_u32(vp);
                 const uint32_t pcol = tmem + kColP + 64 * sb;
-                if (nk == kTileKeys) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t dv = sdesc_sw128(v0 + kk * 2048, kHalf, 1024);
-                        if (elect_one()) mma_bf16_ts(tmem + kColO, pcol + 8 * kk, dv, idesc_pv, !(j == 0 && kk == 0));
-                        __syncwarp();
-                    }
-                } else {
+                if (elect_one()) {   // one lane issues the tile's MMAs and their commits
                     for (int kk = 0; kk < nk / 16; ++kk) {
                         const uint64_t dv = sdesc_sw128(v0 + kk * 2048, kHalf, 1024);
-                        if (elect_one()) mma_bf16_ts(tmem + kColO, pcol + 8 * kk, dv, idesc_pv, !(j == 0 && kk == 0));
-                        __syncwarp();
+                        mma_bf16_ts(tmem + kColO, pcol + 8 * kk, dv, idesc_pv, !(j == 0 && kk == 0));
                     }
-                }
-                if (elect_one()) {
                     mma_commit(&bar.p_free[sb]);
                     mma_commit(&bar.v_empty[vst]);
                     if (j == ntiles - 1) mma_commit(&bar.o_full);
